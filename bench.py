@@ -1,0 +1,499 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV attention path on GB300.
+
+One step = one Qwen3-0.6B-shaped decode step of every decoder layer: for each
+of 28 layers, write the 256 new tokens' K/V into that layer's paged cache
+(kv_cache_write) and run decode attention over batch 256 with context
+lengths uniform in [100, 2048] (paged_attn_decode); 16 query / 8 kv heads,
+head_dim 128, block_size 256, shuffled block tables.  Inputs are synthetic
+and seeded (seed 3042); every layer has its own cache, so each layer's
+working set (about 1.2 GB) is far larger than L2 and no flush is needed.
+
+Printed: one JSON line (rank 0).  `value` is the algorithmic HBM bytes of the
+whole step (decode K/V/q/out/metadata plus the KV write's reads and writes)
+divided by the step time.  `roofline` reports the dominant call
+(paged_attn_decode) against the measured HBM copy bandwidth.  Extra lines of
+the same object report other workloads (graph-padded decode, 8B-shaped
+decode, prefill TFLOP/s, the 32768-token KV write).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+`--impl reference` times the fp64 CPU oracle (the only reference
+implementation of this path) on a bounded sample of the same workload.
+Multi-GPU runs are independent replicas (the path has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn HBM GB/s (% of 8 TB/s); prefill TFLOP/s; KV-write GB/s"
+LAYERS = 28
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def decode_bytes(ctx: np.ndarray, hq: int, hkv: int, d: int = 128, bs: int = 256) -> int:
+    """Algorithmic bytes of one decode call: K and V rows of every context
+    token, q in, out back, block-table entries and context lengths."""
+    L = ctx.astype(np.int64)
+    kv = int(L.sum()) * hkv * d * 2 * 2
+    qo = ctx.size * hq * d * 2 * 2
+    meta = int(((L + bs - 1) // bs).sum()) * 4 + ctx.size * 4
+    return kv + qo + meta
+
+
+def write_bytes(slots: np.ndarray, hkv: int, d: int = 128) -> int:
+    """Algorithmic bytes of one KV write: K and V rows read and written for
+    every non-padding token, plus the slot mapping."""
+    n = int((slots >= 0).sum())
+    return n * hkv * d * 2 * 2 * 2 + slots.size * 4
+
+
+def prefill_flops(w: W.PrefillWorkload) -> int:
+    """4 * D * Hq flops per (query, visible key) pair (QK^T and PV)."""
+    n = w.seqlens_q.astype(np.int64)
+    L = w.seqlens_k.astype(np.int64)
+    c = L - n
+    pairs = int((n * c + n * (n + 1) // 2).sum())
+    return 4 * w.head_dim * w.num_q_heads * pairs
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_decode_layer_rate(min_seconds: float = 10.0, max_reps: int = 20):
+    """Time the fp64 oracle (write + decode) on one layer of the decode
+    workload on the host cores; returns (GB/s of the same algorithmic bytes,
+    threads, description)."""
+    import oracle
+    w = W.qwen3_0p6b_decode()
+    nbytes = decode_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads) + write_bytes(w.slot_mapping, w.num_kv_heads)
+    reps, t_total = 0, 0.0
+    while reps < max_reps and (t_total < min_seconds or reps == 0):
+        kc, vc = w.k_cache.copy(), w.v_cache.copy()
+        t0 = time.perf_counter()
+        oracle.kv_cache_write(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+        oracle.paged_attn_decode(w.q, kc, vc, w.context_lens, w.block_tables, w.scale)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    gbs = nbytes * reps / t_total / 1e9
+    desc = (f"one of the 28 layers (batch 256, full KV write + decode), repeated {reps}x in "
+            f"{t_total:.1f} s; GB/s of the same algorithmic bytes")
+    return gbs, oracle.num_threads(), desc
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return 0
+    import oracle
+    w = W.qwen3_0p6b_decode()
+    # Bounded sample: the first 32 sequences of one layer (write + decode).
+    B = 32
+    nbytes = decode_bytes(w.context_lens[:B], w.num_q_heads, w.num_kv_heads) + \
+        write_bytes(w.slot_mapping[:B], w.num_kv_heads)
+
+    def step():
+        kc, vc = w.k_cache.copy(), w.v_cache.copy()
+        t0 = time.perf_counter()
+        oracle.kv_cache_write(w.k_new[:B], w.v_new[:B], w.slot_mapping[:B], kc, vc)
+        oracle.paged_attn_decode(w.q[:B], kc, vc, w.context_lens[:B], w.block_tables[:B], w.scale)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = nbytes / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "qwen3_0.6b_decode_b256 (sample: 32 of 256 sequences, 1 of 28 layers)",
+                   "batch": 256, "layers": LAYERS, "num_q_heads": 16, "num_kv_heads": 8, "head_dim": 128,
+                   "block_size": 256},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "32 of 256 sequences of one layer, KV write + decode per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def make_cache(torch, num_layers, nb, hkv, gen, device):
+    """The global cache (2, layers, num_blocks, 256, hkv, 128), N(0,1) bf16."""
+    kv = torch.empty((2, num_layers, nb, 256, hkv, 128), dtype=torch.bfloat16, device=device)
+    flat = kv.view(-1)
+    chunk = 1 << 28
+    for lo in range(0, flat.numel(), chunk):
+        hi = min(flat.numel(), lo + chunk)
+        flat[lo:hi] = torch.randn(hi - lo, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    return kv
+
+
+def run_pkv(args, rank, world, local):
+    import torch
+    import paged_kv_cache_304_gb300 as pkv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    pk, peak_kind = peaks()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(3042 + rank)
+
+    w = W.qwen3_0p6b_decode(fill_caches=False)
+    B, hq, hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, 128
+    kv = make_cache(torch, LAYERS, w.num_blocks, hkv, gen, device)
+    qs = torch.randn((LAYERS, B, hq, d), generator=gen, device=device).to(torch.bfloat16)
+    ks = torch.randn((LAYERS, B, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+    vs = torch.randn((LAYERS, B, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+    outs = torch.empty_like(qs)
+    slots = torch.from_numpy(w.slot_mapping).to(device)
+    ctx = torch.from_numpy(w.context_lens).to(device)
+    tab = torch.from_numpy(w.block_tables).to(device)
+    ws = pkv.decode_workspace(B, hq, device)
+    maxctx = w.max_context_len
+    stream = torch.cuda.current_stream(device)
+
+    dec_events = []
+
+    def step(record: bool):
+        for l in range(LAYERS):
+            pkv.kv_cache_write(ks[l], vs[l], slots, kv[0, l], kv[1, l])
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            pkv.paged_attn_decode(qs[l], kv[0, l], kv[1, l], ctx, tab, w.scale, out=outs[l], workspace=ws,
+                                  max_context_len=maxctx)
+            if record:
+                e1.record(stream)
+                dec_events.append((e0, e1))
+
+    for _ in range(max(3, args.warmup)):
+        step(False)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == [], "device error during warm-up"
+
+    step_bytes = LAYERS * (decode_bytes(w.context_lens, hq, hkv) + write_bytes(w.slot_mapping, hkv))
+    dec_bytes = decode_bytes(w.context_lens, hq, hkv)
+
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms, world, device)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_events)
+    clk = clocks.summary()
+
+    # end to end: per-step inputs from pinned host memory, outputs back to host
+    h_q = qs.cpu().pin_memory()
+    h_k = ks.cpu().pin_memory()
+    h_v = vs.cpu().pin_memory()
+    h_meta = [torch.from_numpy(a).pin_memory() for a in (w.slot_mapping, w.context_lens, w.block_tables)]
+    h_out = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
+    d_q, d_k, d_v, d_out = (torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0]),
+                            torch.empty_like(outs[0]))
+    d_meta = [torch.empty_like(t, device=device) for t in h_meta]
+
+    def e2e_step():
+        for dst, src in zip(d_meta, h_meta):
+            dst.copy_(src, non_blocking=True)
+        for l in range(LAYERS):
+            d_q.copy_(h_q[l], non_blocking=True)
+            d_k.copy_(h_k[l], non_blocking=True)
+            d_v.copy_(h_v[l], non_blocking=True)
+            pkv.kv_cache_write(d_k, d_v, d_meta[0], kv[0, l], kv[1, l])
+            pkv.paged_attn_decode(d_q, kv[0, l], kv[1, l], d_meta[1], d_meta[2], w.scale, out=d_out, workspace=ws,
+                                  max_context_len=maxctx)
+            h_out[l].copy_(d_out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    h2d = sum(t.numel() * t.element_size() for t in h_meta) + LAYERS * (
+        h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2)
+    d2h = LAYERS * h_out[0].numel() * 2
+
+    extra = {}
+    if not args.no_extra:
+        extra = run_extras(torch, pkv, device, gen, pk)
+    assert pkv.device_error() == [], "device error during the benchmark"
+
+    value = step_bytes * world / (ms / 1e3) / 1e9
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "qwen3_0.6b_decode_b256: 28 layers x (kv_cache_write + paged_attn_decode)",
+                   "batch": B, "context_lens": "U[100, 2048], seed 3042", "layers": LAYERS, "num_q_heads": hq,
+                   "num_kv_heads": hkv, "head_dim": d, "block_size": 256, "num_blocks_per_layer": w.num_blocks,
+                   "l2": "inputs larger than L2 (about 1.2 GB per layer, a different cache per layer)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(dec_gbs / NOMINAL_HBM_GBS, 4),
+                     "kernel": "paged_attn_decode (decode_kernel + decode_combine_kernel)",
+                     "bytes_per_launch": dec_bytes, "ms_per_launch": round(dec_ms, 5), "traffic": None},
+        "clocks": clk,
+        "e2e": {"value": round(step_bytes * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * LAYERS * 3,
+        "extra": extra,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, desc = oracle_decode_layer_rate()
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _time_calls(torch, fn, reps: int, warm: int = 3):
+    stream = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) for x, y in times)
+
+
+def _decode_extra(torch, pkv, device, gen, w: W.DecodeWorkload, pk, reps=20):
+    kv = make_cache(torch, 1, w.num_blocks, w.num_kv_heads, gen, device)
+    q = torch.randn(w.q.shape, generator=gen, device=device).to(torch.bfloat16)
+    ctx = torch.from_numpy(w.context_lens).to(device)
+    tab = torch.from_numpy(w.block_tables).to(device)
+    ws = pkv.decode_workspace(w.batch, w.num_q_heads, device)
+    out = torch.empty_like(q)
+    ms = _time_calls(torch, lambda: pkv.paged_attn_decode(q, kv[0, 0], kv[1, 0], ctx, tab, w.scale, out=out,
+                                                          workspace=ws, max_context_len=w.max_context_len), reps)
+    nbytes = decode_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del kv
+    return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "bytes": nbytes}
+
+
+def _write_extra(torch, pkv, device, gen, w, pk, reps=20):
+    kv = make_cache(torch, 1, w.num_blocks, w.num_kv_heads, gen, device)
+    k = torch.randn(w.k_new.shape, generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn(w.v_new.shape, generator=gen, device=device).to(torch.bfloat16)
+    slots = torch.from_numpy(w.slot_mapping).to(device)
+    # the write's own working set is smaller than L2: flush L2 between reps
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def fn():
+        pkv.kv_cache_write(k, v, slots, kv[0, 0], kv[1, 0])
+
+    for _ in range(3):
+        fn()
+    times = []
+    stream = torch.cuda.current_stream()
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.median(x.elapsed_time(y) for x, y in times)
+    nbytes = write_bytes(w.slot_mapping, w.num_kv_heads)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del kv
+    return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "bytes": nbytes, "l2": "flushed between reps (256 MB write)"}
+
+
+def _prefill_extra(torch, pkv, device, gen, w: W.PrefillWorkload, pk, reps=10):
+    kv = make_cache(torch, 1, w.num_blocks, w.num_kv_heads, gen, device)
+    q = torch.randn(w.q.shape, generator=gen, device=device).to(torch.bfloat16)
+    cq = torch.from_numpy(w.cu_seqlens_q).to(device)
+    ck = torch.from_numpy(w.cu_seqlens_k).to(device)
+    tab = torch.from_numpy(w.block_tables).to(device)
+    out = torch.empty_like(q)
+    try:
+        ms = _time_calls(torch, lambda: pkv.paged_attn_prefill(q, kv[0, 0], kv[1, 0], cq, ck, tab, w.scale,
+                                                               w.max_seqlen_q, w.max_seqlen_k, out=out), reps)
+    except pkv.PkvError as e:
+        return {"unavailable": str(e)}
+    flops = prefill_flops(w)
+    tf = flops / (ms / 1e3) / 1e12
+    del kv
+    return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_of_measured_bf16": round(tf / pk["bf16_tflops"], 4),
+            "flops": flops}
+
+
+def run_extras(torch, pkv, device, gen, pk):
+    out = {}
+    out["graph_padded_decode_b500_pad512"] = _decode_extra(torch, pkv, device, gen,
+                                                            W.graph_padded_decode(fill_caches=False), pk)
+    out["qwen3_8b_decode_b64"] = _decode_extra(torch, pkv, device, gen, W.qwen3_8b_decode(fill_caches=False), pk)
+    out["tiny_decode_b4_latency"] = _decode_extra(torch, pkv, device, gen, W.tiny_decode(fill_caches=False), pk)
+    out["kv_write_qwen3_8b_prefill_32768_tokens"] = _write_extra(torch, pkv, device, gen,
+                                                                 W.qwen3_8b_prefill(fill_caches=False), pk)
+    out["chunked_prefill_prefix_budget16384"] = _prefill_extra(torch, pkv, device, gen,
+                                                               W.chunked_prefill_prefix(fill_caches=False), pk)
+    out["qwen3_8b_prefill_4x8192"] = _prefill_extra(torch, pkv, device, gen, W.qwen3_8b_prefill(fill_caches=False),
+                                                    pk)
+    torch.cuda.empty_cache()
+    return out
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_pkv(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

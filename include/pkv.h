@@ -1,0 +1,193 @@
+/*
+ * pkv.h -- C ABI of the paged-KV attention library (libpkv.so, sm_103a).
+ *
+ * The library implements the per-decoder-layer paged-KV attention path of the
+ * minimal vLLM-style engine nano-vllm, as described on the page
+ * "13. 读一个最小推理引擎：nano-vllm" (commit bb823b3):
+ *
+ *   1. pkv_kv_cache_write      -- scatter each scheduled token's K and V into
+ *                                 the paged cache by slot; slot -1 is skipped.
+ *   2. pkv_paged_attn_prefill  -- causal GQA attention of a varlen batch whose
+ *                                 sequences may be chunked or prefix-cached,
+ *                                 reading K/V through block tables.
+ *   3. pkv_paged_attn_decode   -- one-query-token GQA attention over a batch,
+ *                                 reading K/V through block tables.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - bf16 tensors are passed as pointers to raw bfloat16 bit patterns
+ *   (pkv_bf16).  Integer metadata is int32.
+ * - Every pointer argument is a DEVICE pointer owned by the caller.  The
+ *   library never allocates, frees or retains memory.  Scratch memory, where a
+ *   call needs some, is passed in by the caller (`workspace`), sized by the
+ *   matching *_workspace_bytes function.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *   asynchronous on that stream; they never synchronise the host and never
+ *   read device data on the host, so they can be captured in a CUDA graph.
+ * - The cache of one layer is a pair of tensors k_cache, v_cache of shape
+ *   (num_blocks, block_size, num_kv_heads, head_dim), C-contiguous
+ *   (page section "第五站：执行准备与 KV 容量": one preallocated cache of shape
+ *   (2, layers, blocks, block_size, kv_heads, head_dim); one layer's K or V is
+ *   one slice of it).  Logical position p of a sequence with block table row
+ *   `bt` lives at slot bt[p / block_size] * block_size + p % block_size
+ *   (same section, slot mapping).
+ * - Supported shapes: block_size == 256 (the page's default, "第二站"),
+ *   head_dim == 128, num_kv_heads in [1, 8], num_q_heads a multiple of
+ *   num_kv_heads with group size num_q_heads / num_kv_heads in [1, 16], and
+ *   num_q_heads <= 64.  Other shapes return PKV_ERR_UNSUPPORTED.
+ * - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * - Return value: PKV_OK, or a negative pkv_status for a host-side argument
+ *   error (nothing is launched) or a launch error.  Faults inside a kernel
+ *   surface at the caller's next synchronisation.  Invalid device-side values
+ *   that the host cannot see (an out-of-range slot or block id, a bounded wait
+ *   that timed out) never fault: the offending access is skipped or clamped
+ *   and a bit is set in the library's device error word, readable with
+ *   pkv_device_error().
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the C ABI are exported even when the library is built with
+ * hidden default visibility. */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef uint16_t pkv_bf16; /* raw bfloat16 bit pattern */
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = -1,        /* a required pointer is NULL */
+  PKV_ERR_SHAPE = -2,       /* inconsistent or negative sizes */
+  PKV_ERR_UNSUPPORTED = -3, /* shape outside the supported set (see above) */
+  PKV_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than required */
+  PKV_ERR_CUDA = -5,        /* a CUDA runtime/driver call or launch failed */
+  PKV_ERR_ALIGN = -6        /* a pointer or stride breaks 16-byte alignment */
+} pkv_status;
+
+/* Bits of the device error word (pkv_device_error). */
+#define PKV_DEVERR_SLOT_RANGE 0x1u   /* kv write: slot < -1 or >= num_blocks*block_size */
+#define PKV_DEVERR_BLOCK_RANGE 0x2u  /* a block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_LEN_RANGE 0x4u    /* a context/sequence length outside its stated bound */
+#define PKV_DEVERR_WAIT_TIMEOUT 0x8u /* a bounded pipeline wait gave up */
+
+/* Human-readable name of a status code.  Never NULL. */
+PKV_API const char* pkv_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+PKV_API int pkv_version(void);
+
+/*
+ * KV-cache write (page section "第六站：注意力层": before attention, in
+ * prefill and decode alike, a small kernel copies every scheduled token's K
+ * and V into the paged cache; slot -1 marks CUDA-graph padding and is
+ * skipped).
+ *
+ *   k, v           [num_tokens, num_kv_heads, head_dim] bf16; token i's row
+ *                  of num_kv_heads*head_dim contiguous elements starts at
+ *                  element i * k_token_stride (resp. v_token_stride).
+ *                  Strides are in elements, >= num_kv_heads*head_dim.
+ *   slot_mapping   [num_tokens] int32: destination slot of token i, or -1.
+ *                  Slots of one call must be distinct (duplicate slots give
+ *                  an unspecified one of the rows).  Out-of-range slots are
+ *                  skipped and flag PKV_DEVERR_SLOT_RANGE.
+ *   k_cache, v_cache  (num_blocks, block_size, num_kv_heads, head_dim) bf16,
+ *                  modified in place: row `slot` receives token i's row
+ *                  bit-exactly; every other element is left untouched.
+ * Pointers and strides must give 16-byte aligned rows (PKV_ERR_ALIGN
+ * otherwise).  num_tokens == 0 is a no-op.
+ */
+PKV_API int pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16* v,
+                       int64_t v_token_stride, const int32_t* slot_mapping, int32_t num_tokens,
+                       pkv_bf16* k_cache, pkv_bf16* v_cache, int32_t num_blocks, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_dim, void* stream);
+
+/*
+ * Scratch bytes pkv_paged_attn_decode needs for `batch` sequences on the
+ * current CUDA device (it depends on the device's SM count).
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim);
+
+/*
+ * Decode attention (page section "第六站：注意力层": decode attends from one
+ * new token per sequence to that sequence's history, reading it from the
+ * paged cache through the block table; "第五站": CUDA-graph pad rows).
+ *
+ *   q             [batch, num_q_heads, head_dim] bf16, 16-byte aligned.
+ *   k_cache, v_cache  as in pkv_kv_cache_write (already holding the new
+ *                 token: call pkv_kv_cache_write first).
+ *   context_lens  [batch] int32: L_b, the tokens of sequence b to attend to,
+ *                 the new one included.  L_b == 0 marks a pad row: its output
+ *                 is zeros and nothing is read for it.  L_b must be <=
+ *                 max_context_len and <= max_blocks_per_seq * block_size.
+ *   block_tables  [batch, max_blocks_per_seq] int32, row b lists sequence b's
+ *                 physical blocks in logical order; entries at index
+ *                 >= ceil(L_b / block_size) are never read.
+ *   scale         multiplies q.k before the softmax (usually 1/sqrt(head_dim)).
+ *   out           [batch, num_q_heads, head_dim] bf16:
+ *                 out[b,h] = sum_t softmax_t(scale * q[b,h].K[t]) V[t], with
+ *                 K, V the kv head h / (num_q_heads/num_kv_heads) rows of the
+ *                 first L_b logical positions.  Accumulation is fp32; the
+ *                 probabilities are rounded to bf16 before the V product.
+ *   workspace     >= pkv_decode_workspace_bytes(batch, num_q_heads, head_dim)
+ *                 device bytes, 256-byte aligned, contents need not be
+ *                 initialised; overwritten by the call.  Two calls that may
+ *                 run concurrently need two workspaces.
+ */
+PKV_API int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                          const int32_t* context_lens, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, int32_t max_context_len, float scale, pkv_bf16* out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Varlen causal prefill attention (page sections "第二站" -- every step
+ * computes from num_cached_tokens onward; "第三站" -- only the first sequence
+ * of a step may be a split chunk; "第六站" -- with prefix hits or a chunk
+ * continuation the block table is passed so the whole context is read from
+ * the paged cache).
+ *
+ *   q             [total_q, num_q_heads, head_dim] bf16, packed: sequence i
+ *                 owns rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1.
+ *   cu_seqlens_q  [num_seqs+1] int32, cu_seqlens_q[0] == 0, n_i = difference.
+ *   cu_seqlens_k  [num_seqs+1] int32, L_i = difference = tokens of sequence i
+ *                 in the cache after the write (cached + new).
+ *                 c_i = L_i - n_i >= 0 is num_cached_tokens; query row j of
+ *                 sequence i sits at position c_i + j and attends to keys
+ *                 0 .. c_i + j (causal mask aligned bottom-right).
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32.
+ *   max_seqlen_q, max_seqlen_k  host-known upper bounds of n_i and L_i.
+ *   out           [total_q, num_q_heads, head_dim] bf16.
+ * Accumulation is fp32; probabilities are rounded to bf16 before the V
+ * product.  total_q == 0 is a no-op.
+ */
+PKV_API int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                           int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                           pkv_bf16* out, void* stream);
+
+/*
+ * Read (and, if `clear` is nonzero, reset) the device error word of the
+ * current device.  Synchronises the device.  *out receives an OR of
+ * PKV_DEVERR_* bits set by kernels since the last clear.
+ */
+PKV_API int pkv_device_error(uint32_t* out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,98 @@
+// kv_write.cu -- KV-cache write: scatter each scheduled token's K and V row
+// into the paged cache at its slot, skipping slot -1 (CUDA-graph padding).
+//
+// Page "13. 读一个最小推理引擎：nano-vllm", section "第六站：注意力层": before
+// attention, in prefill and decode alike, every scheduled token's K and V are
+// copied into the paged cache; a slot of -1 is a padding row and is skipped.
+//
+// The work is a pure copy, bound by HBM: per token, 2 x row_bytes read and
+// 2 x row_bytes written (row_bytes = num_kv_heads * head_dim * 2 = 2 KiB for
+// 8 kv heads of 128).  Each thread moves one 16-byte chunk of K and the
+// matching chunk of V per iteration with 128-bit loads (read-once, no L1
+// allocation) and 128-bit stores, so a warp covers 512 contiguous bytes of a
+// row.  The grid is a multiple of the SM count and strides over all chunks.
+#include <cuda_runtime.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+__device__ unsigned int g_err_kv_write;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// One 16-byte chunk of K and of V per (token, chunk) pair.  `row_vecs` chunks
+// make one token row; strides are in 16-byte chunks.
+__global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__ k, int64_t k_stride,
+                                                       const uint4* __restrict__ v, int64_t v_stride,
+                                                       const int32_t* __restrict__ slots,
+                                                       int32_t num_tokens, uint4* __restrict__ k_cache,
+                                                       uint4* __restrict__ v_cache, int64_t num_slots,
+                                                       int32_t row_vecs) {
+  // num_tokens * row_vecs < 2^31 is checked by the launcher, so 32-bit
+  // index arithmetic (cheap unsigned division) is exact here.
+  const uint32_t total = static_cast<uint32_t>(num_tokens) * static_cast<uint32_t>(row_vecs);
+  const uint32_t step = gridDim.x * blockDim.x;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += step) {
+    const uint32_t t = i / static_cast<uint32_t>(row_vecs);
+    const uint32_t c = i - t * static_cast<uint32_t>(row_vecs);
+    const int64_t s = __ldg(slots + t);
+    if (s == -1) continue;
+    if (s < 0 || s >= num_slots) {
+      if (c == 0) atomicOr(&g_err_kv_write, PKV_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const uint4 kv = ld_stream(k + static_cast<int64_t>(t) * k_stride + c);
+    const uint4 vv = ld_stream(v + static_cast<int64_t>(t) * v_stride + c);
+    k_cache[s * row_vecs + c] = kv;
+    v_cache[s * row_vecs + c] = vv;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_cache_write(const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                                  int64_t v_stride, const int32_t* slots, int32_t num_tokens,
+                                  uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,
+                                  int32_t row_elems, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int32_t row_vecs = row_elems / 8;  // 8 bf16 per 16-byte chunk
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  const int64_t chunks = static_cast<int64_t>(num_tokens) * row_vecs;
+  if (chunks >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  int64_t blocks = (chunks + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread blocks per SM
+  if (blocks > cap) blocks = cap;
+  kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      reinterpret_cast<const uint4*>(k), k_stride / 8, reinterpret_cast<const uint4*>(v), v_stride / 8,
+      slots, num_tokens, reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache),
+      num_slots, row_vecs);
+  return cudaGetLastError();
+}
+
+cudaError_t read_error_kv_write(uint32_t* out, bool clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err_kv_write, sizeof v);
+  if (e != cudaSuccess) return e;
+  *out = v;
+  if (clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_err_kv_write, &zero, sizeof zero);
+  }
+  return e;
+}
+
+}  // namespace pkv

@@ -1,0 +1,208 @@
+// pkv_api.cu -- the C ABI declared in include/pkv.h: host-side argument
+// validation, TMA tensor-map construction and kernel launch.  Nothing here
+// allocates device memory or synchronises the host (pkv_device_error aside).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kDecodeTileTokens = 16;  // must match kT in decode.cu
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor maps over one layer's K and V caches, (num_blocks, 256, Hkv, 128)
+// bf16, for tiles of `tile_tokens` consecutive tokens of one block.  The
+// preferred map is 5-D over (dim within half, token, head, dim half, block)
+// so that one copy brings a tile of every head, laid out as
+// [half][head][token][64 dims] with 128-byte swizzled rows.  If the driver
+// refuses that stride order, a 3-D map over (dim, head, slot) is used and
+// the kernel issues one copy per (half, head) into the same layout.
+bool encode_cache_maps(const void* k_cache, const void* v_cache, int num_blocks, int hkv,
+                       int tile_tokens, CacheMaps* maps) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(hkv) * kHeadDim * 2;  // bytes per token row
+  {
+    cuuint64_t dims[5] = {64, kBlockSize, static_cast<cuuint64_t>(hkv), 2, static_cast<cuuint64_t>(num_blocks)};
+    cuuint64_t strides[4] = {row, kHeadDim * 2, 128, row * kBlockSize};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tile_tokens), static_cast<cuuint32_t>(hkv), 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r1 = enc(&maps->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(k_cache), dims, strides,
+                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r2 = enc(&maps->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(v_cache), dims, strides,
+                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS) {
+      maps->per_head = 0;
+      return true;
+    }
+  }
+  cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  cuuint64_t strides[2] = {kHeadDim * 2, row};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tile_tokens)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r1 = enc(&maps->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k_cache), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r2 = enc(&maps->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v_cache), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  maps->per_head = 1;
+  return r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS;
+}
+
+// Shape checks shared by the two attention calls.
+int check_attn_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                     int32_t num_blocks, int32_t max_blocks_per_seq, float scale) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PKV_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_SHAPE;
+  if (head_dim != kHeadDim || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (num_kv_heads > kMaxKvHeads || num_q_heads > kMaxQHeads) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * kBlockSize >= (int64_t{1} << 31)) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: inconsistent or negative sizes";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: shape outside the supported set";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing or too small";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA call or kernel launch failed";
+    case PKV_ERR_ALIGN: return "PKV_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    default: return "unknown pkv status";
+  }
+}
+
+int pkv_version(void) { return 100; }
+
+int pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16* v, int64_t v_token_stride,
+                       const int32_t* slot_mapping, int32_t num_tokens, pkv_bf16* k_cache, pkv_bf16* v_cache,
+                       int32_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                       void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_SHAPE;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_token_stride < row || v_token_stride < row) return PKV_ERR_SHAPE;
+  if (row % 8 || k_token_stride % 8 || v_token_stride % 8) return PKV_ERR_ALIGN;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+  const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
+  if (static_cast<int64_t>(num_tokens) * (row / 8) >= (int64_t{1} << 31)) return PKV_ERR_UNSUPPORTED;
+  cudaError_t e = launch_kv_cache_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, k_cache,
+                                        v_cache, num_slots, static_cast<int32_t>(row),
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim) {
+  (void)head_dim;
+  if (batch < 0 || num_q_heads <= 0) return 0;
+  const int sms = sm_count();
+  if (sms <= 0) return 0;
+  return decode_workspace_bytes(batch, num_q_heads, sms);
+}
+
+int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                          const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                          pkv_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
+  int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  if (st != PKV_OK) return st;
+  if (max_context_len >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !context_lens || !block_tables || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+  const int sms = sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  if (!workspace || workspace_bytes < decode_workspace_bytes(batch, num_q_heads, sms)) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGN;
+  CacheMaps maps;
+  if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kDecodeTileTokens, &maps))
+    return PKV_ERR_CUDA;
+  DecodeArgs a;
+  a.q = q;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.out = out;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.max_context_len = max_context_len;
+  a.scale = scale;
+  a.workspace = workspace;
+  cudaError_t e = launch_paged_attn_decode(a, maps, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                           int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale, pkv_bf16* out, void* stream) {
+  (void)q; (void)k_cache; (void)v_cache; (void)cu_seqlens_q; (void)cu_seqlens_k; (void)block_tables;
+  (void)max_blocks_per_seq; (void)num_seqs; (void)total_q; (void)max_seqlen_q; (void)max_seqlen_k;
+  (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)block_size; (void)num_blocks; (void)scale;
+  (void)out; (void)stream;
+  return PKV_ERR_UNSUPPORTED;
+}
+
+int pkv_device_error(uint32_t* out, int clear) {
+  if (!out) return PKV_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+  uint32_t a = 0, b = 0;
+  if (read_error_kv_write(&a, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
+  if (read_error_decode(&b, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
+  *out = a | b;
+  return PKV_OK;
+}
+
+}  // extern "C"

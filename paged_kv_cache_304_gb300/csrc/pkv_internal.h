@@ -1,0 +1,79 @@
+// pkv_internal.h -- launchers shared between the C-ABI front end (pkv_api.cu)
+// and the kernel translation units.  Arguments here are already validated.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 256;
+constexpr int kHeadDim = 128;
+constexpr int kMaxKvHeads = 8;
+constexpr int kMaxGroup = 16;
+constexpr int kMaxQHeads = 64;
+
+// ---- KV write
+cudaError_t launch_kv_cache_write(const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                                  int64_t v_stride, const int32_t* slots, int32_t num_tokens,
+                                  uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,
+                                  int32_t row_elems, cudaStream_t stream);
+
+// ---- decode
+struct DecodeArgs {
+  const uint16_t* q;
+  const int32_t* context_lens;
+  const int32_t* block_tables;
+  uint16_t* out;
+  int32_t max_blocks_per_seq;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  int32_t max_context_len;
+  float scale;
+  void* workspace;
+};
+// Tensor maps over the caches, built by the front end (see pkv_api.cu).
+// `per_head` selects the layout of the copy: one 5-D box per K (or V) tile,
+// or 2 * num_kv_heads 3-D boxes with the same shared-memory image.
+struct CacheMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+  int per_head;
+};
+size_t decode_workspace_bytes(int batch, int num_q_heads, int num_sms);
+int decode_grid(int num_sms);
+cudaError_t launch_paged_attn_decode(const DecodeArgs& a, const CacheMaps& maps, int num_sms,
+                                     cudaStream_t stream);
+
+// ---- prefill
+struct PrefillArgs {
+  const uint16_t* q;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* block_tables;
+  uint16_t* out;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t total_q;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  float scale;
+};
+cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv_maps,
+                                      const CUtensorMap& q_map, int num_sms, cudaStream_t stream);
+
+// ---- device error words (one per translation unit)
+cudaError_t read_error_kv_write(uint32_t* out, bool clear);
+cudaError_t read_error_decode(uint32_t* out, bool clear);
+cudaError_t read_error_prefill(uint32_t* out, bool clear);
+
+}  // namespace pkv
