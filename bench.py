@@ -233,6 +233,8 @@ def make_cache(torch, num_layers, nb, hkv, gen, device):
 
 
 def run_pkv(args, rank, world, local):
+    global LAYERS
+    LAYERS = args.layers
     import torch
     import paged_kv_cache_304_gb300 as pkv
 
@@ -488,6 +490,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="decoder layers per step (28 for the benchmark; 1 for a small profiling case)")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
