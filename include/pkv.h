@@ -180,6 +180,40 @@ PKV_API int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, c
                            pkv_bf16* out, void* stream);
 
 /*
+ * Decode attention without caller scratch: the same computation and
+ * arguments as pkv_paged_attn_decode, minus `workspace`/`workspace_bytes`.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory themselves -- for example a plugin inside a
+ * host engine that owns every device allocation and forbids plugins from
+ * allocating once serving has started, or a C caller that only holds the raw
+ * tensor pointers it was handed.  Such callers cannot obtain the workspace
+ * pkv_paged_attn_decode asks for.
+ *
+ * Scratch lives in one fixed array inside the library, PKV_DECODE_STATIC_SCRATCH_BYTES
+ * (8 MiB) per GPU, held by every GPU that loads the library until the process
+ * exits.  A call whose batch needs more than that
+ * (pkv_decode_workspace_bytes(batch, num_q_heads, head_dim) > 8 MiB, e.g.
+ * batch above 855 at 16 query heads on a 152-SM GPU) returns PKV_ERR_WORKSPACE
+ * and launches nothing.  The call allocates nothing and frees nothing.
+ *
+ * The first call on a device looks up that array's device address (with the
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array and it keeps the
+ * previous call's contents; no part of it needs to start at zero.  Calls
+ * that can overlap on the GPU (different streams without ordering between
+ * them) race on the array and give undefined results: order them, or use
+ * pkv_paged_attn_decode with one workspace per stream.
+ */
+#define PKV_DECODE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+PKV_API int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache,
+                                          const pkv_bf16* v_cache, const int32_t* context_lens,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                          int32_t max_context_len, float scale, pkv_bf16* out,
+                                          void* stream);
+
+/*
  * Read (and, if `clear` is nonzero, reset) the device error word of the
  * current device.  Synchronises the device.  *out receives an OR of
  * PKV_DEVERR_* bits set by kernels since the last clear.

@@ -195,6 +195,70 @@ int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv
   return PKV_ERR_UNSUPPORTED;
 }
 
+// ---------------------------------------------------------------------------
+// Decode without caller scratch.  For callers that cannot allocate device
+// memory (a plugin whose host engine owns all allocations, a C caller holding
+// only the pointers it was given): the split-K partials go to one fixed
+// library-owned array instead of a caller workspace.  Nothing here allocates.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Fixed scratch of the no-allocation decode call: one copy per GPU that loads
+// the library, alive until the process exits.  Its name is only a host-side
+// stand-in; kernels get the device address looked up below.
+static __device__ __align__(256) uint8_t g_decode_static_scratch[PKV_DECODE_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevicesCached = 64;
+std::mutex g_static_scratch_mutex;
+void* g_static_scratch_ptr[kMaxDevicesCached] = {};
+
+// Device address of the fixed scratch on the current device, looked up once
+// per device (with that device current) and cached.  nullptr on failure.
+void* static_scratch_for_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+  if (!g_static_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_static_scratch) != cudaSuccess) return nullptr;
+    g_static_scratch_ptr[dev] = ptr;
+  }
+  return g_static_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                                  const int32_t* context_lens, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  int32_t max_context_len, float scale, pkv_bf16* out, void* stream) {
+  if (batch < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
+  int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  if (st != PKV_OK) return st;
+  if (max_context_len >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  // Reject batches whose partials do not fit the fixed array, before launching.
+  const size_t need = decode_workspace_bytes(batch, num_q_heads, sms);
+  if (need > PKV_DECODE_STATIC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  void* scratch = static_scratch_for_current_device();
+  if (!scratch) return PKV_ERR_CUDA;
+  // Nothing in the scratch must start at zero: every partial and every
+  // per-sequence record the combine step reads is written earlier in the
+  // same call.
+  return pkv_paged_attn_decode(q, k_cache, v_cache, context_lens, block_tables, max_blocks_per_seq, batch,
+                               num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
+                               out, scratch, PKV_DECODE_STATIC_SCRATCH_BYTES, stream);
+}
+
 int pkv_device_error(uint32_t* out, int clear) {
   if (!out) return PKV_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
