@@ -15,7 +15,8 @@
 namespace pkv {
 namespace {
 
-constexpr int kDecodeTileTokens = 16;  // must match kT in decode.cu
+constexpr int kDecodeTileTokens = 16;    // must match kT in decode.cu
+constexpr int kPrefillTileTokens = 128;  // must match kTileN in prefill.cu
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -41,21 +42,22 @@ int sm_count() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tensor maps over one layer's K and V caches, (num_blocks, 256, Hkv, 128)
-// bf16, for tiles of `tile_tokens` consecutive tokens of one block.  The
+// bf16, for tiles of `tile_tokens` consecutive tokens of one block and
+// `heads_per_box` kv heads (all heads for decode, one for prefill).  The
 // preferred map is 5-D over (dim within half, token, head, dim half, block)
-// so that one copy brings a tile of every head, laid out as
+// so that one copy brings the whole tile, laid out as
 // [half][head][token][64 dims] with 128-byte swizzled rows.  If the driver
 // refuses that stride order, a 3-D map over (dim, head, slot) is used and
 // the kernel issues one copy per (half, head) into the same layout.
 bool encode_cache_maps(const void* k_cache, const void* v_cache, int num_blocks, int hkv,
-                       int tile_tokens, CacheMaps* maps) {
+                       int tile_tokens, int heads_per_box, CacheMaps* maps) {
   auto enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t row = static_cast<cuuint64_t>(hkv) * kHeadDim * 2;  // bytes per token row
   {
     cuuint64_t dims[5] = {64, kBlockSize, static_cast<cuuint64_t>(hkv), 2, static_cast<cuuint64_t>(num_blocks)};
     cuuint64_t strides[4] = {row, kHeadDim * 2, 128, row * kBlockSize};
-    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tile_tokens), static_cast<cuuint32_t>(hkv), 2, 1};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tile_tokens), static_cast<cuuint32_t>(heads_per_box), 2, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     CUresult r1 = enc(&maps->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(k_cache), dims, strides,
                       box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -164,7 +166,7 @@ int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_
   if (!workspace || workspace_bytes < decode_workspace_bytes(batch, num_q_heads, sms)) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGN;
   CacheMaps maps;
-  if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kDecodeTileTokens, &maps))
+  if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kDecodeTileTokens, num_kv_heads, &maps))
     return PKV_ERR_CUDA;
   DecodeArgs a;
   a.q = q;
@@ -188,11 +190,48 @@ int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv
                            int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
                            int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t block_size, int32_t num_blocks, float scale, pkv_bf16* out, void* stream) {
-  (void)q; (void)k_cache; (void)v_cache; (void)cu_seqlens_q; (void)cu_seqlens_k; (void)block_tables;
-  (void)max_blocks_per_seq; (void)num_seqs; (void)total_q; (void)max_seqlen_q; (void)max_seqlen_k;
-  (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)block_size; (void)num_blocks; (void)scale;
-  (void)out; (void)stream;
-  return PKV_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PKV_ERR_SHAPE;
+  int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  if (st != PKV_OK) return st;
+  if (max_seqlen_q > max_seqlen_k) return PKV_ERR_SHAPE;
+  if (num_seqs > 65535 || max_seqlen_q > (1 << 22) || max_seqlen_k >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
+  if (total_q == 0 || num_seqs == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+  auto enc = encode_fn();
+  if (!enc) return PKV_ERR_CUDA;
+  CUtensorMap qmap;
+  {
+    // q [total_q, Hq, 128]: boxes of 128 rows x 64 dims of one head, swizzled.
+    cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
+    cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(num_q_heads) * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<pkv_bf16*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  }
+  CacheMaps maps;
+  if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kPrefillTileTokens, 1, &maps))
+    return PKV_ERR_CUDA;
+  PrefillArgs a;
+  a.q = q;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.block_tables = block_tables;
+  a.out = out;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  cudaError_t e = launch_paged_attn_prefill(a, maps, qmap, sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------
@@ -262,10 +301,11 @@ int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, co
 int pkv_device_error(uint32_t* out, int clear) {
   if (!out) return PKV_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   if (read_error_kv_write(&a, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (read_error_decode(&b, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
-  *out = a | b;
+  if (read_error_prefill(&c, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
+  *out = a | b | c;
   return PKV_OK;
 }
 

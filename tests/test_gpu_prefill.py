@@ -1,0 +1,124 @@
+"""Varlen causal prefill attention on the GPU vs the fp64 oracle.
+
+Each case writes the step's new tokens with the library's KV write (checked
+bit-exact), runs prefill through the C ABI and compares with the oracle:
+every output element at sizes the oracle finishes quickly, sampled rows (the
+first and last rows of every sequence plus a seeded sample) at the
+8B-shaped 4 x 8192 size.  Bar: max-abs <= 2e-2, mean-abs <= 2e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_304_gb300 as pkv
+import workloads as W
+from tests.gpu_util import check_close, i32, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(w: W.PrefillWorkload, rows=None, cu_q=None, q=None):
+    """Write + prefill on the GPU; compare with the oracle on `rows`."""
+    cu_q = w.cu_seqlens_q if cu_q is None else cu_q
+    q = w.q if q is None else q
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    nq = np.diff(cu_q)
+    out = pkv.paged_attn_prefill(to_dev(q), kc, vc, i32(cu_q), i32(w.cu_seqlens_k), i32(w.block_tables), w.scale,
+                                 int(nq.max()) if nq.size else 0, w.max_seqlen_k)
+    torch.cuda.synchronize()
+    okc, ovc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_cache_write(w.k_new, w.v_new, w.slot_mapping, okc, ovc)
+    assert np.array_equal(to_host(kc), okc) and np.array_equal(to_host(vc), ovc), "kv write not bit-exact"
+    ref = oracle.paged_attn_prefill(q, okc, ovc, cu_q, w.cu_seqlens_k, w.block_tables, w.scale, rows=rows)
+    got = to_host(out)
+    res = check_close(got, ref, w.name, rows=rows)
+    assert pkv.device_error() == []
+    return res, got, ref
+
+
+def test_prefill_chunked_prefix_budget16384():
+    """33 admitted prompts, a split first sequence, 9 prefix-cache hits."""
+    run_prefill(W.chunked_prefill_prefix())
+
+
+def test_prefill_qwen3_8b_4x8192_sampled_rows():
+    w = W.qwen3_8b_prefill()
+    rng = np.random.default_rng(8192)
+    rows = []
+    for i in range(w.num_seqs):
+        lo, hi = int(w.cu_seqlens_q[i]), int(w.cu_seqlens_q[i + 1])
+        rows += [lo, lo + 1, lo + 127, lo + 128, hi - 129, hi - 1]
+        rows += list(rng.integers(lo, hi, size=26))
+    run_prefill(w, rows=np.unique(np.array(rows)))
+
+
+EDGE = [
+    # (lengths, cached)
+    ([1], [0]),
+    ([2, 1, 3], [1, 0, 0]),
+    ([127, 128, 129], [0, 0, 0]),
+    ([255, 256, 257], [0, 0, 0]),
+    ([300, 600], [255, 256]),
+    ([513, 700, 1000], [257, 1, 511]),
+    ([1025, 40], [896, 0]),
+    ([2000], [1000]),
+]
+
+
+@pytest.mark.parametrize("lens,cached", EDGE, ids=[f"case{i}" for i in range(len(EDGE))])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8)])
+def test_prefill_edges(lens, cached, hq, hkv):
+    need = sum(-(-L // 256) for L in lens)
+    w = W.make_prefill("edge", 700 + sum(lens), lens, cached, hq, hkv, num_blocks=need + 3)
+    run_prefill(w)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 1), (64, 8), (12, 4), (4, 2)])
+def test_prefill_group_sizes(hq, hkv):
+    lens, cached = [700, 130, 1], [300, 0, 0]
+    w = W.make_prefill("groups", 800 + hq + hkv, lens, cached, hq, hkv, num_blocks=10)
+    run_prefill(w)
+
+
+def test_prefill_empty_sequence_in_batch():
+    """A sequence with no new tokens (n = 0) in the middle of the batch."""
+    w = W.make_prefill("empty_mid", 811, [300, 200, 150], [10, 0, 20], 16, 8, num_blocks=8)
+    n = np.diff(w.cu_seqlens_q)
+    keep = np.r_[np.arange(w.cu_seqlens_q[0], w.cu_seqlens_q[1]), np.arange(w.cu_seqlens_q[2], w.cu_seqlens_q[3])]
+    cu_q = np.array([0, n[0], n[0], n[0] + n[2]], np.int32)
+    # sequence 1 keeps its keys in the cache (written below) but asks for no rows
+    run_prefill(w, cu_q=cu_q, q=w.q[keep])
+
+
+def test_prefill_single_token_matches_decode():
+    """A prefill of one new token per sequence is a decode step: both GPU
+    paths agree with the oracle (and hence with each other)."""
+    lens = [1, 257, 600, 1300]
+    w = W.make_prefill("onetoken", 812, lens, [L - 1 for L in lens], 16, 8, num_blocks=12)
+    _, got_p, ref = run_prefill(w)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    out_d = pkv.paged_attn_decode(to_dev(w.q), kc, vc, i32(np.array(lens, np.int32)), i32(w.block_tables), w.scale)
+    check_close(to_host(out_d), ref, "decode on prefill inputs")
+
+
+def test_prefill_scale_and_permuted_blocks():
+    w = W.make_prefill("scale", 813, [900, 333], [0, 100], 16, 8, num_blocks=12)
+    w.scale = 0.7 / math.sqrt(128)
+    run_prefill(w)
+
+
+def test_prefill_repeat_is_deterministic():
+    w = W.make_prefill("repeat", 814, [1000, 500], [0, 0], 16, 8, num_blocks=8)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    args = (to_dev(w.q), kc, vc, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables), w.scale,
+            w.max_seqlen_q, w.max_seqlen_k)
+    a = to_host(pkv.paged_attn_prefill(*args))
+    b = to_host(pkv.paged_attn_prefill(*args))
+    assert np.array_equal(a, b)
