@@ -87,9 +87,14 @@ def prefill_flops(w: W.PrefillWorkload) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Started before the warm-up (nvidia-smi takes a while to come up) and
+    summarised over the samples whose timestamps fall inside the timed
+    region (mark_start / mark_end); if none does, over the nearest ones.
+    """
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -97,16 +102,26 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 8.0
+            while time.time() < deadline and os.path.getsize(self.file.name) == 0:
+                time.sleep(0.05)
         except (OSError, ValueError):
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -116,6 +131,16 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         if self.proc is None or self.file is None:
             return None
@@ -124,17 +149,29 @@ class ClockSampler:
         with open(self.file.name) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) >= 10:
+                    rows.append((self._ts(parts[0]), parts[1:]))
         os.unlink(self.file.name)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        inside = [r for t, r in rows if t is not None and self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        if not inside and self.t0 is not None:
+            mid = (self.t0 + (self.t1 or self.t0)) / 2
+            timed = [(abs(t - mid), r) for t, r in rows if t is not None]
+            inside = [r for _, r in sorted(timed, key=lambda x: x[0])[:2]] if timed else [r for _, r in rows]
+        use = inside or [r for _, r in rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in use) if v is not None]
+        mx = [v for v in (num(r[2]) for r in use) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(use)}
 
 
 def dist_env():
@@ -275,23 +312,24 @@ def run_pkv(args, rank, world, local):
                 e1.record(stream)
                 dec_events.append((e0, e1))
 
-    for _ in range(max(3, args.warmup)):
-        step(False)
-    torch.cuda.synchronize()
-    assert pkv.device_error() == [], "device error during warm-up"
-
     step_bytes = LAYERS * (decode_bytes(w.context_lens, hq, hkv) + write_bytes(w.slot_mapping, hkv))
     dec_bytes = decode_bytes(w.context_lens, hq, hkv)
 
     with ClockSampler(local) as clocks:
+        for _ in range(max(3, args.warmup)):
+            step(False)
+        torch.cuda.synchronize()
+        assert pkv.device_error() == [], "device error during warm-up"
         barrier(world)
         torch.cuda.synchronize()
+        clocks.mark_start()
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for _ in range(args.steps):
             step(True)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         barrier(world)
     ms = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms, world, device)
@@ -482,6 +520,47 @@ def run_extras(torch, pkv, device, gen, pk):
     return out
 
 
+CASES = ("step", "prefill_8b", "prefill_chunked", "decode_8b", "decode_padded", "decode_tiny", "write_32768")
+
+
+def run_case(args, local):
+    """One workload on its own (for profiling): time it and print one JSON line."""
+    import torch
+    import paged_kv_cache_304_gb300 as pkv
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    pk, peak_kind = peaks()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(3040)
+    reps = max(1, args.steps)
+    if args.case == "prefill_8b":
+        n = args.prefill_seqs
+        if n == 4:
+            w = W.qwen3_8b_prefill(fill_caches=False)
+        else:  # a smaller pool for profiling runs
+            w = W.make_prefill(f"qwen3_8b_prefill_{n}x8192", 3045, [8192] * n, [0] * n, 32, 8,
+                               num_blocks=32 * n + 8, fill_caches=False)
+        res = _prefill_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    elif args.case == "prefill_chunked":
+        w = W.chunked_prefill_prefix(fill_caches=False)
+        res = _prefill_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    elif args.case == "decode_8b":
+        w = W.qwen3_8b_decode(fill_caches=False)
+        res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    elif args.case == "decode_padded":
+        w = W.graph_padded_decode(fill_caches=False)
+        res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    elif args.case == "decode_tiny":
+        w = W.tiny_decode(fill_caches=False)
+        res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    else:
+        w = W.qwen3_8b_prefill(fill_caches=False)
+        res = _write_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    assert pkv.device_error() == [], "device error"
+    print(json.dumps({"case": args.case, "workload": w.name, "peak_kind": peak_kind, **res}), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,12 +569,17 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--case", choices=CASES, default="step",
+                    help="step (the benchmark) or one workload on its own, for profiling")
+    ap.add_argument("--prefill-seqs", type=int, default=4, help="sequences of 8192 tokens for --case prefill_8b")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="decoder layers per step (28 for the benchmark; 1 for a small profiling case)")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.case != "step":
+        return run_case(args, local)
     return run_pkv(args, rank, world, local)
 
 

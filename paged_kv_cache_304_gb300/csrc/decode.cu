@@ -437,6 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
   const Smem sm = carve(base, p);
   const int warp = threadIdx.x >> 5;
+  griddep_wait();
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -456,32 +458,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the per-CTA partials of sequences that straddle CTAs; zero pad rows.
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p, int grid) {
-  const int b = blockIdx.x;
+// One warp per (sequence, query head); lane i handles dims 4i .. 4i+3.
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(const DecodeParams p, int grid) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int pair = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (pair >= p.B * p.Hq) return;
+  const int b = pair / p.Hq, hq = pair - b * p.Hq;
+  const int lane = threadIdx.x & 31;
   const int L = clamp_len(__ldg(p.ctx + b), p.lmax);
-  uint16_t* o = p.out + static_cast<int64_t>(b) * p.Hq * kHeadDim;
-  const int n = p.Hq * kHeadDim;
+  uint16_t* o = p.out + static_cast<int64_t>(pair) * kHeadDim + 4 * lane;
   if (L == 0) {
-    for (int i = threadIdx.x; i < n / 8; i += blockDim.x) reinterpret_cast<uint4*>(o)[i] = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
     return;
   }
   const int2 meta = p.ws_meta[b];
   const int c0 = max(0, meta.x), c1 = min(grid - 1, meta.y);
   if (c1 <= c0) return;  // finished inside one CTA
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int hq = i >> 7;
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_ml[static_cast<int64_t>(b + c) * p.Hq + hq].x);
-    float lsum = 0.f, acc = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-      const int64_t slot = b + c;
-      const float2 ml = p.ws_ml[slot * p.Hq + hq];
-      const float wgt = fast_exp2(ml.x - M);
-      lsum += wgt * ml.y;
-      acc += wgt * p.ws_o[slot * n + i];
-    }
-    o[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc / lsum));
+  float M = -INFINITY;
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_ml[static_cast<int64_t>(b + c) * p.Hq + hq].x);
+  float lsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = c0; c <= c1; ++c) {
+    const int64_t row = static_cast<int64_t>(b + c) * p.Hq + hq;
+    const float2 ml = p.ws_ml[row];
+    const float wgt = fast_exp2(ml.x - M);
+    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + row * kHeadDim + 4 * lane);
+    lsum += wgt * ml.y;
+    acc.x += wgt * v.x;
+    acc.y += wgt * v.y;
+    acc.z += wgt * v.z;
+    acc.w += wgt * v.w;
   }
+  const float inv = 1.f / lsum;
+  *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
@@ -540,11 +552,11 @@ cudaError_t launch_paged_attn_decode(const DecodeArgs& a, const CacheMaps& maps,
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  decode_kernel<<<grid, 32 * (a.num_kv_heads + 1), smem, stream>>>(maps.k, maps.v, p);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_kernel, dim3(grid), dim3(32 * (a.num_kv_heads + 1)), smem, stream, maps.k, maps.v, p);
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<a.batch, 256, 0, stream>>>(p, grid);
-  return cudaGetLastError();
+  const int pairs = a.batch * a.num_q_heads;
+  return launch_pdl(decode_combine_kernel, dim3((pairs + kCombineWarps - 1) / kCombineWarps),
+                    dim3(32 * kCombineWarps), 0, stream, p, grid);
 }
 
 cudaError_t read_error_decode(uint32_t* out, bool clear) {

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
                                                        int32_t num_tokens, uint4* __restrict__ k_cache,
                                                        uint4* __restrict__ v_cache, int64_t num_slots,
                                                        int32_t row_vecs) {
+  griddep_wait();
+  griddep_launch_dependents();
   // num_tokens * row_vecs < 2^31 is checked by the launcher, so 32-bit
   // index arithmetic (cheap unsigned division) is exact here.
   const uint32_t total = static_cast<uint32_t>(num_tokens) * static_cast<uint32_t>(row_vecs);
@@ -76,11 +78,10 @@ cudaError_t launch_kv_cache_write(const uint16_t* k, int64_t k_stride, const uin
   int64_t blocks = (chunks + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread blocks per SM
   if (blocks > cap) blocks = cap;
-  kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      reinterpret_cast<const uint4*>(k), k_stride / 8, reinterpret_cast<const uint4*>(v), v_stride / 8,
-      slots, num_tokens, reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache),
-      num_slots, row_vecs);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    reinterpret_cast<const uint4*>(k), k_stride / 8, reinterpret_cast<const uint4*>(v),
+                    v_stride / 8, slots, num_tokens, reinterpret_cast<uint4*>(k_cache),
+                    reinterpret_cast<uint4*>(v_cache), num_slots, row_vecs);
 }
 
 cudaError_t read_error_kv_write(uint32_t* out, bool clear) {

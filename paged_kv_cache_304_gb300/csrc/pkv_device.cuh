@@ -136,6 +136,18 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch.  griddep_wait() blocks until the kernel
+// that precedes this one in the stream has completed and its memory is
+// visible (a no-op when that kernel did not opt in); griddep_launch_dependents()
+// lets the next kernel in the stream be scheduled early, so its launch and
+// set-up overlap this kernel's tail.  Every kernel of the library waits
+// before it touches global memory, so stream order is preserved.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- math
 // 2^x on the SFU (PTX ex2.approx; ex2(-inf) = +0).
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "pkv.h"
 
@@ -16,6 +17,25 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxKvHeads = 8;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxQHeads = 64;
+
+// Launch `kernel` on `stream` with programmatic stream serialization
+// allowed, so it may start while the previous kernel drains (each kernel
+// calls griddepcontrol.wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- KV write
 cudaError_t launch_kv_cache_write(const uint16_t* k, int64_t k_stride, const uint16_t* v,

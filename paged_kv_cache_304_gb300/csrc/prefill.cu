@@ -126,6 +126,8 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const CUten
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int h = blockIdx.x;    // query head
   const int seq = blockIdx.y;  // sequence
   const int q0 = __ldg(p.cu_q + seq), q1 = __ldg(p.cu_q + seq + 1);
@@ -393,8 +395,7 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
   if (e != cudaSuccess) return e;
   const int max_tiles = (a.max_seqlen_q + kTileM - 1) / kTileM;
   dim3 grid(a.num_q_heads, a.num_seqs, max_tiles);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kv.k, kv.v, p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kv.k, kv.v, p);
 }
 
 cudaError_t read_error_prefill(uint32_t* out, bool clear) {
