@@ -60,6 +60,25 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
+def recorded_traffic():
+    """DRAM bytes per decode_kernel launch from the committed ncu capture,
+    or None if the kernel's sources changed since it was taken."""
+    import hashlib
+    rec = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+    srcs = [os.path.join(ROOT, "paged_kv_cache_304_gb300", "csrc", f) for f in ("decode.cu", "pkv_device.cuh")]
+    try:
+        vals = {}
+        with open(rec) as f:
+            for line in f:
+                if line.strip() and not line.startswith("#"):
+                    k, v = line.split(None, 1)
+                    vals[k] = v.strip()
+        h = hashlib.sha256(b"".join(open(p, "rb").read() for p in srcs)).hexdigest()
+        return int(vals["bytes_per_launch"]) if vals.get("sources_sha256") == h else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def decode_bytes(ctx: np.ndarray, hq: int, hkv: int, d: int = 128, bs: int = 256) -> int:
     """Algorithmic bytes of one decode call: K and V rows of every context
     token, q in, out back, block-table entries and context lengths."""
@@ -403,7 +422,8 @@ def run_pkv(args, rank, world, local):
                      "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(dec_gbs / NOMINAL_HBM_GBS, 4),
                      "kernel": "paged_attn_decode (decode_kernel + decode_combine_kernel)",
-                     "bytes_per_launch": dec_bytes, "ms_per_launch": round(dec_ms, 5), "traffic": None},
+                     "bytes_per_launch": dec_bytes, "ms_per_launch": round(dec_ms, 5),
+                     "traffic": recorded_traffic() if LAYERS == 28 or LAYERS == 1 else None},
         "clocks": clk,
         "e2e": {"value": round(step_bytes * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
