@@ -8,24 +8,29 @@
 // is read from the paged cache).  Query row j of sequence i sits at position
 // c_i + j, c_i = L_i - n_i, and sees keys 0 .. c_i + j.
 //
-// Design (one CTA = one 128-row query tile of one query head):
-// * warp 0, producer: TMA-loads the Q tile once, then streams the 128-token
-//   K and V tiles of the kv head (two per 256-token cache block, looked up in
-//   the block table) into 2-stage rings.  Tiles are stored as two 64-dim
-//   halves of 128 rows x 128 bytes with the 128-byte swizzle.
+// Design.  One CTA = one 128-row query tile of one sequence for TWO query
+// heads of the same kv group ("slots" A and B): both read the same K/V tiles
+// under the same causal mask, so every K/V byte brought into shared memory
+// feeds twice the tensor work, and the two slots ping-pong so the tensor
+// pipe always has one slot's work while the other slot's softmax runs.
+// * warp 0, producer: TMA-loads the two Q tiles, then streams the kv head's
+//   128-token K and V tiles (two per 256-token cache block, looked up in the
+//   block table) into 2-stage rings, as 64-dim halves of 128 rows x 128 bytes
+//   with the 128-byte swizzle.
 // * warp 1, MMA: one thread issues tcgen05.mma (kind::f16, bf16 in, fp32
-//   accumulate in tensor memory).  S_j = Q K_j^T goes to one of two TMEM
-//   buffers (so S_{j+1} overlaps the softmax of S_j); O += P_j V_j
-//   accumulates in a third TMEM region.  tcgen05.commit signals mbarriers.
-// * warps 4-7, softmax: thread r owns query row r = TMEM lane r.  It loads its
-//   128 scores with tcgen05.ld, applies the causal mask on diagonal tiles,
-//   keeps a running row maximum (in log2 units, scale * log2(e) folded in)
-//   and row sum, writes P in bf16 to shared memory in the layout the PV MMA
-//   reads, and rescales O in TMEM only when its row maximum grew by more than
-//   2^8 (otherwise the stale maximum stays the reference; p <= 256 then).
-//   At the end it normalises O by the row sum and stores bf16 rows.
+//   accumulate).  Tensor memory holds S_A | S_B | O_A | O_B (128 columns
+//   each).  Order per K/V tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1); the
+//   probabilities P_X(j) are written over S_X(j) as packed bf16 and read as
+//   the A operand straight from tensor memory.
+// * warps 2-5 (slot A) and 6-9 (slot B), softmax: warp w reads TMEM lanes
+//   32 (w % 4) .. +31, so thread r of a group owns query row r (TMEM lane r).  It loads its 128 scores with tcgen05.ld, applies the
+//   causal mask on diagonal tiles, keeps the running row maximum (log2
+//   units, scale * log2(e) folded in; reductions split over 8 independent
+//   accumulators), rescales O in tensor memory only when the maximum grew by
+//   more than 2^8, and stores P.  At the end it normalises O by the row sum
+//   and writes bf16 rows.
 // * Tiles are launched heaviest first (the last query tile of a sequence
-//   sees the most keys).
+//   sees the most keys); the hardware block scheduler balances the rest.
 // Every wait is bounded (two seconds); on timeout the CTA flags
 // PKV_DEVERR_WAIT_TIMEOUT, frees its tensor memory and returns.
 #include <cuda_runtime.h>
@@ -38,64 +43,56 @@ namespace {
 
 __device__ unsigned int g_err_prefill;
 
-constexpr int kTileM = 128;       // query rows per CTA
-constexpr int kTileN = 128;       // keys per K/V tile
+constexpr int kTileM = 128;    // query rows per slot
+constexpr int kTileN = 128;    // keys per K/V tile
 constexpr int kKvStages = 2;
-constexpr int kThreads = 256;     // 8 warps: producer, MMA, 2 idle, 4 softmax
-constexpr uint32_t kTileBytes = kTileN * kHeadDim * 2;  // 32 KiB: one Q, K, V or P tile
-constexpr uint32_t kHalfBytes = kTileBytes / 2;         // one 64-dim (or 64-key) half
-constexpr uint32_t kTmemCols = 512;                     // S0 | S1 | O | unused
-constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTileM, kTileN, 0);    // B = K, K-major
-constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 1);  // B = V, N-major
+constexpr int kThreads = 320;  // 10 warps: producer, MMA, 4 softmax A, 4 softmax B
+constexpr uint32_t kTileBytes = kTileN * kHeadDim * 2;  // 32 KiB: one Q, K or V tile
+constexpr uint32_t kHalfBytes = kTileBytes / 2;         // one 64-dim half
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kTileM, kTileN, 0);    // B = K tile, K-major
+constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 1);  // B = V tile, N-major
 
 struct PrefillParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   const int32_t* tables;
   uint16_t* out;
-  int32_t maxb, S, Hq, Hkv, G, num_blocks, total_q, per_half;
+  int32_t maxb, S, Hq, Hkv, G, npairs, num_blocks, total_q, per_half;
   float sl2;  // scale * log2(e)
 };
 
+// Shared memory: Q_A | Q_B | K stages | V stages | barriers.
 struct Smem {
-  uint8_t* q;       // kTileBytes
-  uint8_t* k0;      // kKvStages K tiles, kTileBytes apart
-  uint8_t* v0;      // kKvStages V tiles, kTileBytes apart
-  uint8_t* p;       // kTileBytes
+  uint8_t* q;   // 2 tiles
+  uint8_t* k0;  // kKvStages tiles
+  uint8_t* v0;  // kKvStages tiles
   uint64_t* q_full;
   uint64_t* k_full;   // [kKvStages]
-  uint64_t* k_empty;
-  uint64_t* v_full;
-  uint64_t* v_empty;
-  uint64_t* s_full;   // [2]
-  uint64_t* s_empty;  // [2]
-  uint64_t* p_full;
-  uint64_t* o_done;
+  uint64_t* k_empty;  // [kKvStages]
+  uint64_t* v_full;   // [kKvStages]
+  uint64_t* v_empty;  // [kKvStages]
+  uint64_t* s_full;   // [2 slots]
+  uint64_t* p_full;   // [2 slots]
+  uint64_t* o_done;   // [2 slots]
   uint32_t* tmem_base;
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* base) {
   Smem s;
-  uint8_t* c = base;
-  s.q = c;
-  c += kTileBytes;
-  s.k0 = c;
-  c += kKvStages * kTileBytes;
-  s.v0 = c;
-  c += kKvStages * kTileBytes;
-  s.p = c;
-  c += kTileBytes;
-  uint64_t* b = reinterpret_cast<uint64_t*>(c);
+  s.q = base;
+  s.k0 = base + 2 * kTileBytes;
+  s.v0 = s.k0 + kKvStages * kTileBytes;
+  uint64_t* b = reinterpret_cast<uint64_t*>(s.v0 + kKvStages * kTileBytes);
   s.q_full = b;
   s.k_full = b + 1;
-  s.k_empty = b + 1 + kKvStages;
-  s.v_full = b + 1 + 2 * kKvStages;
-  s.v_empty = b + 1 + 3 * kKvStages;
-  s.s_full = b + 1 + 4 * kKvStages;
-  s.s_empty = s.s_full + 2;
-  s.p_full = s.s_empty + 2;
-  s.o_done = s.p_full + 1;
-  s.tmem_base = reinterpret_cast<uint32_t*>(s.o_done + 1);
+  s.k_empty = s.k_full + kKvStages;
+  s.v_full = s.k_empty + kKvStages;
+  s.v_empty = s.v_full + kKvStages;
+  s.s_full = s.v_empty + kKvStages;
+  s.p_full = s.s_full + 2;
+  s.o_done = s.p_full + 2;
+  s.tmem_base = reinterpret_cast<uint32_t*>(s.o_done + 2);
   return s;
 }
 
@@ -110,7 +107,7 @@ __device__ __forceinline__ int load_block(const PrefillParams& p, int seq, int l
   return phys;
 }
 
-// Load one 128-token K or V tile (all 128 dims of kv head g) into `dst` as two
+// One 128-token K or V tile (all 128 dims of kv head g) into `dst` as two
 // swizzled 64-dim halves.
 __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const CUtensorMap* map, uint8_t* dst,
                                              uint64_t* bar, int phys, int tin, int g) {
@@ -123,20 +120,44 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const CUten
   }
 }
 
+// S = Q K^T: A = Q tile, B = K tile, both K-major (dims contiguous) with the
+// 128-byte swizzle; k-step kk selects 32 bytes of a 64-dim half.
+__device__ __forceinline__ void issue_s(uint32_t d, uint32_t qa, uint32_t ka) {
+#pragma unroll
+  for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    tc::mma_ss(d, tc::smem_desc_sw128(qa + off, 16, 1024), tc::smem_desc_sw128(ka + off, 16, 1024), kIdescS,
+               kk > 0);
+  }
+}
+
+// O += P V with P (128 x 128 keys, packed bf16) in tensor memory at `p_tmem`
+// and V (keys x dims, dims contiguous) in shared memory: 64-dim halves are
+// 16 KiB apart (leading offset), 8-key groups 1 KiB apart (stride offset).
+__device__ __forceinline__ void issue_pv(uint32_t o, uint32_t p_tmem, uint32_t va, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kTileN / 16; ++kk)
+    tc::mma_ts(o, p_tmem + kk * 8, tc::smem_desc_sw128(va + kk * 2048, kHalfBytes, 1024), kIdescPV,
+               (acc || kk > 0) ? 1u : 0u);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   griddep_wait();
   griddep_launch_dependents();
-  const int h = blockIdx.x;    // query head
-  const int seq = blockIdx.y;  // sequence
+  const int g = blockIdx.x / p.npairs;   // kv head
+  const int pair = blockIdx.x - g * p.npairs;
+  const int hA = g * p.G + 2 * pair;      // query head of slot A
+  const bool has_b = 2 * pair + 1 < p.G;  // slot B: query head hA + 1
+  const int seq = blockIdx.y;
   const int q0 = __ldg(p.cu_q + seq), q1 = __ldg(p.cu_q + seq + 1);
   const int k0 = __ldg(p.cu_k + seq), k1 = __ldg(p.cu_k + seq + 1);
   const int n = q1 - q0, L = k1 - k0;
   const int c = L - n;
   if (n <= 0) return;
   if (c < 0 || L > p.maxb * kBlockSize || q1 > p.total_q || q0 < 0) {
-    if (threadIdx.x == 0) atomicOr(&g_err_prefill, PKV_DEVERR_LEN_RANGE);
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_err_prefill, PKV_DEVERR_LEN_RANGE);
     return;
   }
   const int ntiles = (n + kTileM - 1) / kTileM;
@@ -144,9 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicOr(&g_err_prefill, PKV_DEVERR_LEN_RANGE);  // n exceeds the stated max_seqlen_q
   if (static_cast<int>(blockIdx.z) >= ntiles) return;
   const int m = ntiles - 1 - static_cast<int>(blockIdx.z);  // heaviest tile first
-  const int g = h / p.G;
-  const int row_end = min(kTileM * (m + 1), n);              // exclusive, tile-local rows < row_end - 128m
-  const int kv_end = c + row_end;                            // keys 0 .. kv_end-1 are visible to some row
+  const int row_end = min(kTileM * (m + 1), n);
+  const int kv_end = c + row_end;  // keys 0 .. kv_end-1 are visible to some row
   const int nkv = (kv_end + kTileN - 1) / kTileN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -165,10 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_empty[i], 4);
+      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.o_done[i], 1);
     }
-    mbar_init(sm.p_full, 4);
-    mbar_init(sm.o_done, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -179,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *sm.tmem_base;
-  const uint32_t tmem_s0 = tmem, tmem_s1 = tmem + 128, tmem_o = tmem + 256;
+  // columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -187,10 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      mbar_arrive_expect_tx(sm.q_full, kTileBytes);
       const int row0 = q0 + kTileM * m;
-      tma_load_3d(sm.q, &qmap, sm.q_full, 0, h, row0);
-      tma_load_3d(sm.q + kHalfBytes, &qmap, sm.q_full, 64, h, row0);
+      mbar_arrive_expect_tx(sm.q_full, has_b ? 2 * kTileBytes : kTileBytes);
+      tma_load_3d(sm.q, &qmap, sm.q_full, 0, hA, row0);
+      tma_load_3d(sm.q + kHalfBytes, &qmap, sm.q_full, 64, hA, row0);
+      if (has_b) {
+        tma_load_3d(sm.q + kTileBytes, &qmap, sm.q_full, 0, hA + 1, row0);
+        tma_load_3d(sm.q + kTileBytes + kHalfBytes, &qmap, sm.q_full, 64, hA + 1, row0);
+      }
       int phys = load_block(p, seq, 0);
       int nxt = nkv > 2 ? load_block(p, seq, 1) : 0;
       for (int j = 0; j < nkv; ++j) {
@@ -203,162 +226,188 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tin = (j & 1) * kTileN;
         if (!mbar_wait(&sm.k_empty[st], par, &g_err_prefill)) break;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-        load_kv_tile(p, &kmap, (sm.k0 + st * kTileBytes), &sm.k_full[st], phys, tin, g);
+        load_kv_tile(p, &kmap, sm.k0 + st * kTileBytes, &sm.k_full[st], phys, tin, g);
         if (!mbar_wait(&sm.v_empty[st], par, &g_err_prefill)) break;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-        load_kv_tile(p, &vmap, (sm.v0 + st * kTileBytes), &sm.v_full[st], phys, tin, g);
+        load_kv_tile(p, &vmap, sm.v0 + st * kTileBytes, &sm.v_full[st], phys, tin, g);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      const uint32_t qa = smem_u32(sm.q), pa = smem_u32(sm.p);
-      bool ok = mbar_wait(sm.q_full, 0, &g_err_prefill);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kKvStages, sb = j & 1;
-        if (!mbar_wait(&sm.k_full[st], (j / kKvStages) & 1, &g_err_prefill)) return false;
-        if (!mbar_wait(&sm.s_empty[sb], ((j >> 1) & 1) ^ 1, &g_err_prefill)) return false;
+      const uint32_t qa = smem_u32(sm.q), qb = qa + kTileBytes;
+      const uint32_t sA = tmem, sB = tmem + 128, oA = tmem + 256, oB = tmem + 384;
+      bool ok = mbar_wait(sm.q_full, 0, &g_err_prefill) && mbar_wait(&sm.k_full[0], 0, &g_err_prefill);
+      if (ok) {
         tc::fence_after();
-        const uint32_t ka = smem_u32((sm.k0 + st * kTileBytes));
-        const uint32_t d = sb ? tmem_s1 : tmem_s0;
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          tc::mma_ss(d, tc::smem_desc_sw128(qa + off, 16, 1024), tc::smem_desc_sw128(ka + off, 16, 1024), kIdescS,
-                     kk > 0);
+        const uint32_t ka = smem_u32(sm.k0);
+        issue_s(sA, qa, ka);
+        tc::commit(&sm.s_full[0]);
+        if (has_b) {
+          issue_s(sB, qb, ka);
+          tc::commit(&sm.s_full[1]);
         }
-        tc::commit(&sm.s_full[sb]);
-        tc::commit(&sm.k_empty[st]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
+        tc::commit(&sm.k_empty[0]);
+      }
       for (int j = 0; j < nkv && ok; ++j) {
-        if (j + 1 < nkv && !issue_s(j + 1)) break;
         const int st = j % kKvStages;
-        if (!mbar_wait(sm.p_full, j & 1, &g_err_prefill)) break;
+        const bool more = j + 1 < nkv;
+        const int st1 = (j + 1) % kKvStages;
         if (!mbar_wait(&sm.v_full[st], (j / kKvStages) & 1, &g_err_prefill)) break;
+        if (!mbar_wait(&sm.p_full[0], j & 1, &g_err_prefill)) break;
         tc::fence_after();
-        const uint32_t va = smem_u32((sm.v0 + st * kTileBytes));
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // A = P (rows x keys, keys contiguous); B = V (keys x dims, dims contiguous):
-          // 64-dim halves are 16 KiB apart (leading offset), 8-key groups 1 KiB apart.
-          const uint32_t aoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          tc::mma_ss(tmem_o, tc::smem_desc_sw128(pa + aoff, 16, 1024),
-                     tc::smem_desc_sw128(va + kk * 2048, kHalfBytes, 1024), kIdescPV, (j > 0 || kk > 0));
+        const uint32_t va = smem_u32(sm.v0 + st * kTileBytes);
+        issue_pv(oA, sA, va, j > 0);
+        if (!more) tc::commit(&sm.o_done[0]);
+        if (more) {
+          if (!mbar_wait(&sm.k_full[st1], ((j + 1) / kKvStages) & 1, &g_err_prefill)) break;
+          tc::fence_after();
+          issue_s(sA, qa, smem_u32(sm.k0 + st1 * kTileBytes));
+          tc::commit(&sm.s_full[0]);
         }
-        tc::commit(sm.o_done);
+        if (has_b) {
+          if (!mbar_wait(&sm.p_full[1], j & 1, &g_err_prefill)) break;
+          tc::fence_after();
+          issue_pv(oB, sB, va, j > 0);
+          if (!more) tc::commit(&sm.o_done[1]);
+          if (more) {
+            issue_s(sB, qb, smem_u32(sm.k0 + st1 * kTileBytes));
+            tc::commit(&sm.s_full[1]);
+          }
+        }
         tc::commit(&sm.v_empty[st]);
+        if (more) tc::commit(&sm.k_empty[st1]);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2 && (warp < 6 || has_b)) {
     // ------------------------------------------------------------ softmax + epilogue
+    const int slot = warp >= 6 ? 1 : 0;
+    const int h = hA + slot;
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;                 // tile row = TMEM lane
+    const int r = wq * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const int lim_row = c + kTileM * m + r;        // last visible key of this row
+    const uint32_t s_addr = tmem + slot * 128 + lane_bits;
+    const uint32_t o_addr = tmem + 256 + slot * 128 + lane_bits;
+    const int lim_row = c + kTileM * m + r;  // last visible key of this row
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    const uint32_t prow = smem_u32(sm.p) + r * 128;
     for (int j = 0; j < nkv && ok; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&sm.s_full[sb], (j >> 1) & 1, &g_err_prefill)) {
+      if (!mbar_wait(&sm.s_full[slot], j & 1, &g_err_prefill)) {
         ok = false;
         break;
       }
       tc::fence_after();
-      float s[128];
-      const uint32_t sa = (sb ? tmem_s1 : tmem_s0) + lane_bits;
-      tc::ld32(sa + 0, s + 0);
-      tc::ld32(sa + 32, s + 32);
-      tc::ld32(sa + 64, s + 64);
-      tc::ld32(sa + 96, s + 96);
-      tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
-      // causal mask: key 128 j + x visible iff x <= lim
+      // causal mask: key 128 j + x is visible iff x <= lim.  Only warps that
+      // hold a diagonal row take the masked path; the mask of a 32-key
+      // chunk is a 32-bit word (bit x set iff key x of the chunk is visible).
       const int lim = lim_row - kTileN * j;
-      if (lim < kTileN - 1) {
+      const bool wdiag = __any_sync(0xffffffffu, lim < kTileN - 1);
+      auto chunk_mask = [&](int k0) -> uint32_t {
+        const int nv = lim - k0 + 1;  // visible keys in this chunk
+        return nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+      };
+      // Pass 1: row maximum, two 32-column chunks at a time, 8 accumulators.
+      float mx[8];
 #pragma unroll
-        for (int x = 0; x < 128; ++x)
-          if (x > lim) s[x] = -INFINITY;
+      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+      for (int cp = 0; cp < 2; ++cp) {
+        float a[32], b[32];
+        tc::ld32(s_addr + 64 * cp, a);
+        tc::ld32(s_addr + 64 * cp + 32, b);
+        tc::wait_ld();
+        if (wdiag) {
+          const uint32_t va = chunk_mask(64 * cp), vb = chunk_mask(64 * cp + 32);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const float ea = ((va >> x) & 1u) ? a[x] : -INFINITY;
+            const float eb = ((vb >> x) & 1u) ? b[x] : -INFINITY;
+            mx[x & 7] = fmaxf(mx[x & 7], fmaxf(ea, eb));
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) mx[x & 7] = fmaxf(mx[x & 7], fmaxf(a[x], b[x]));
+        }
       }
-      float mt = s[0];
-#pragma unroll
-      for (int x = 1; x < 128; ++x) mt = fmaxf(mt, s[x]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_ref, mt * p.sl2);
       float alpha = 1.f;
       if (m_new > m_ref + 8.f) {
         alpha = fast_exp2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
         m_ref = m_new;
       }
+      // O_X is stable here: S_X(j) completing implies PV_X(j-1) completed.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tc::ld32(o_addr + cc * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] *= alpha;
+          tc::st32(o_addr + cc * 32, o);
+        }
+      }
       const float mu = m_ref;  // finite: key 0 is visible to every row
-      float rs = 0.f;
-      uint32_t pk[64];
+      // Pass 2: p = 2^(s * scale * log2e - m) for 32 keys at a time, packed to
+      // bf16 pairs and written over S: keys 32q..32q+31 go to columns
+      // 16q..16q+15, which hold keys this pass has already read.
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float cur[32];
+      tc::ld32(s_addr, cur);
+      tc::wait_ld();
 #pragma unroll
-      for (int x = 0; x < 128; x += 2) {
-        const float e0 = fast_exp2(fmaf(s[x], p.sl2, -mu));
-        const float e1 = fast_exp2(fmaf(s[x + 1], p.sl2, -mu));
-        rs += e0 + e1;
-        pk[x >> 1] = pack_bf16x2(e0, e1);
-      }
-      l = l * alpha + rs;
-      // PV_{j-1} must be done before O is rescaled and before P is overwritten.
-      if (j > 0) {
-        if (!mbar_wait(sm.o_done, (j - 1) & 1, &g_err_prefill)) {
-          ok = false;
-          break;
+      for (int q = 0; q < 4; ++q) {
+        float nxt[32];
+        if (q < 3) tc::ld32(s_addr + 32 * (q + 1), nxt);
+        uint32_t pk[16];
+        if (wdiag) {
+          const uint32_t vm = chunk_mask(32 * q);
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (!((vm >> x) & 1u)) cur[x] = -INFINITY;
         }
-        tc::fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t oa = tmem_o + lane_bits;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            tc::ld32(oa + cc * 32, o);
-            tc::wait_ld();
+        for (int x = 0; x < 32; x += 2) {
+          const float e0 = fast_exp2(fmaf(cur[x], p.sl2, -mu));
+          const float e1 = fast_exp2(fmaf(cur[x + 1], p.sl2, -mu));
+          rs[(x >> 1) & 7] += e0 + e1;
+          pk[x >> 1] = pack_bf16x2(e0, e1);
+        }
+        tc::st16u(s_addr + 16 * q, pk);
+        if (q < 3) {
+          tc::wait_ld();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= alpha;
-            tc::st32(oa + cc * 32, o);
-          }
-          tc::wait_st();
+          for (int x = 0; x < 32; ++x) cur[x] = nxt[x];
         }
       }
-      // P row r: keys 0-63 in the first half, 64-127 in the second; 16-byte
-      // chunk q of a 128-byte row is stored at chunk q ^ (r & 7).
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint32_t addr = prow + (q >> 3) * kHalfBytes + ((((q & 7) ^ (r & 7))) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]), "r"(pk[4 * q + 1]),
-                     "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
+      l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
+      tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.p_full);
+      if (lane == 0) mbar_arrive(&sm.p_full[slot]);
     }
-    if (ok && mbar_wait(sm.o_done, (nkv - 1) & 1, &g_err_prefill)) {
+    if (ok && mbar_wait(&sm.o_done[slot], 0, &g_err_prefill)) {
       tc::fence_after();
-      const float inv = 1.f / l;
+      const float inv = fast_rcp(l);
       const int row = kTileM * m + r;
       uint16_t* dst = p.out + (static_cast<int64_t>(q0 + row) * p.Hq + h) * kHeadDim;
-      const uint32_t oa = tmem_o + lane_bits;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float o[32];
-        tc::ld32(oa + cc * 32, o);
+        tc::ld32(o_addr + cc * 32, o);
         tc::wait_ld();
         if (row < n) {
 #pragma unroll
           for (int x = 0; x < 32; x += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(o[x] * inv, o[x + 1] * inv);
-            v.y = pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv);
-            v.z = pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv);
-            v.w = pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + cc * 32 + x) = v;
+            const uint32_t w0 = pack_bf16x2(o[x] * inv, o[x + 1] * inv);
+            const uint32_t w1 = pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv);
+            const uint32_t w2 = pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv);
+            const uint32_t w3 = pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv);
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + cc * 32 + x), "r"(w0), "r"(w1),
+                         "r"(w2), "r"(w3)
+                         : "memory");
           }
         }
       }
@@ -386,6 +435,7 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
   p.Hq = a.num_q_heads;
   p.Hkv = a.num_kv_heads;
   p.G = a.num_q_heads / a.num_kv_heads;
+  p.npairs = (p.G + 1) / 2;
   p.num_blocks = a.num_blocks;
   p.total_q = a.total_q;
   p.per_half = kv.per_head;
@@ -394,7 +444,7 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int max_tiles = (a.max_seqlen_q + kTileM - 1) / kTileM;
-  dim3 grid(a.num_q_heads, a.num_seqs, max_tiles);
+  dim3 grid(a.num_kv_heads * p.npairs, a.num_seqs, max_tiles);
   return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kv.k, kv.v, p);
 }
 
