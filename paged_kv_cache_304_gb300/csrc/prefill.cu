@@ -302,33 +302,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // chunk is a 32-bit word (bit x set iff key x of the chunk is visible).
       const int lim = lim_row - kTileN * j;
       const bool wdiag = __any_sync(0xffffffffu, lim < kTileN - 1);
-      auto chunk_mask = [&](int k0) -> uint32_t {
-        const int nv = lim - k0 + 1;  // visible keys in this chunk
-        return nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
-      };
-      // Pass 1: row maximum, two 32-column chunks at a time, 8 accumulators.
-      float mx[8];
+      // All 128 scores of the row in one tensor-memory round trip.
+      float s[128];
+      tc::ld32(s_addr + 0, s + 0);
+      tc::ld32(s_addr + 32, s + 32);
+      tc::ld32(s_addr + 64, s + 64);
+      tc::ld32(s_addr + 96, s + 96);
+      tc::wait_ld();
+      if (wdiag) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+        for (int q = 0; q < 4; ++q) {
+          const int nv = lim - 32 * q + 1;  // visible keys in chunk q
+          const uint32_t vm = nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {
-        float a[32], b[32];
-        tc::ld32(s_addr + 64 * cp, a);
-        tc::ld32(s_addr + 64 * cp + 32, b);
-        tc::wait_ld();
-        if (wdiag) {
-          const uint32_t va = chunk_mask(64 * cp), vb = chunk_mask(64 * cp + 32);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const float ea = ((va >> x) & 1u) ? a[x] : -INFINITY;
-            const float eb = ((vb >> x) & 1u) ? b[x] : -INFINITY;
-            mx[x & 7] = fmaxf(mx[x & 7], fmaxf(ea, eb));
-          }
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) mx[x & 7] = fmaxf(mx[x & 7], fmaxf(a[x], b[x]));
+          for (int x = 0; x < 32; ++x)
+            if (!((vm >> x) & 1u)) s[32 * q + x] = -INFINITY;
         }
       }
+      float mx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+      for (int x = 8; x < 128; ++x) mx[x & 7] = fmaxf(mx[x & 7], s[x]);
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_ref, mt * p.sl2);
@@ -336,6 +331,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (m_new > m_ref + 8.f) {
         alpha = fast_exp2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
         m_ref = m_new;
+      }
+      const float mu = m_ref;  // finite: key 0 is visible to every row
+      // p = 2^(s * scale * log2e - m), packed to bf16 pairs and written over
+      // S 32 keys at a time: keys 32q..32q+31 go to columns 16q..16q+15, which
+      // hold scores already in registers.
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const float e0 = fast_exp2(fmaf(s[32 * q + x], p.sl2, -mu));
+          const float e1 = fast_exp2(fmaf(s[32 * q + x + 1], p.sl2, -mu));
+          rs[(x >> 1) & 7] += e0 + e1;
+          pk[x >> 1] = pack_bf16x2(e0, e1);
+        }
+        tc::st16u(s_addr + 16 * q, pk);
       }
       // O_X is stable here: S_X(j) completing implies PV_X(j-1) completed.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -347,39 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] *= alpha;
           tc::st32(o_addr + cc * 32, o);
-        }
-      }
-      const float mu = m_ref;  // finite: key 0 is visible to every row
-      // Pass 2: p = 2^(s * scale * log2e - m) for 32 keys at a time, packed to
-      // bf16 pairs and written over S: keys 32q..32q+31 go to columns
-      // 16q..16q+15, which hold keys this pass has already read.
-      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float cur[32];
-      tc::ld32(s_addr, cur);
-      tc::wait_ld();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float nxt[32];
-        if (q < 3) tc::ld32(s_addr + 32 * (q + 1), nxt);
-        uint32_t pk[16];
-        if (wdiag) {
-          const uint32_t vm = chunk_mask(32 * q);
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            if (!((vm >> x) & 1u)) cur[x] = -INFINITY;
-        }
-#pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const float e0 = fast_exp2(fmaf(cur[x], p.sl2, -mu));
-          const float e1 = fast_exp2(fmaf(cur[x + 1], p.sl2, -mu));
-          rs[(x >> 1) & 7] += e0 + e1;
-          pk[x >> 1] = pack_bf16x2(e0, e1);
-        }
-        tc::st16u(s_addr + 16 * q, pk);
-        if (q < 3) {
-          tc::wait_ld();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) cur[x] = nxt[x];
         }
       }
       l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
