@@ -393,9 +393,29 @@ def run_pkv(args, rank, world, local):
         h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2)
     d2h = LAYERS * h_out[0].numel() * 2
 
-    extra = {}
+    # the same step captured once as a CUDA graph (bucket = batch) and replayed
+    from paged_kv_cache_304_gb300.graphs import DecodeGraphRunner
+    runner = DecodeGraphRunner([(kv[0, l], kv[1, l]) for l in range(LAYERS)], hq, w.max_blocks_per_seq, w.scale,
+                               max_batch=B, max_context_len=maxctx, buckets=[B])
+    runner.run(qs, ks, vs, slots, ctx, tab)
+    graph = runner.graphs[B]
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, device)
+    del runner, graph
+
+    extra = {"decode_step_cuda_graph": {"ms_per_step": round(graph_ms, 4),
+                                        "GB/s": round(step_bytes * world / (graph_ms / 1e3) / 1e9, 2),
+                                        "note": "same 28-layer step replayed from one captured CUDA graph"}}
     if not args.no_extra:
-        extra = run_extras(torch, pkv, device, gen, pk)
+        extra.update(run_extras(torch, pkv, device, gen, pk))
     assert pkv.device_error() == [], "device error during the benchmark"
 
     value = step_bytes * world / (ms / 1e3) / 1e9

@@ -160,3 +160,11 @@ def test_cache_fill_history_and_stale():
     used = set(w.block_tables[w.block_tables >= 0].tolist())
     for blk in set(range(w.num_blocks)) - used:
         assert (w.k_cache[blk] == W.SENTINEL_K).all()
+
+
+def test_graph_bucket_sizes_match_the_page():
+    from paged_kv_cache_304_gb300.graphs import graph_batch_sizes
+    sizes = [int(x) for x in golden()["graph_batch_sizes"].split(",")]
+    assert graph_batch_sizes(512) == sizes
+    assert graph_batch_sizes(8) == [1, 2, 4, 8]
+    assert graph_batch_sizes(40) == [1, 2, 4, 8, 16, 32, 40]
