@@ -393,27 +393,38 @@ def run_pkv(args, rank, world, local):
         h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2)
     d2h = LAYERS * h_out[0].numel() * 2
 
-    # the same step captured once as a CUDA graph (bucket = batch) and replayed
+    # the same step with the write fused into decode, and both captured once
+    # as a CUDA graph (bucket = batch) and replayed
     from paged_kv_cache_304_gb300.graphs import DecodeGraphRunner
-    runner = DecodeGraphRunner([(kv[0, l], kv[1, l]) for l in range(LAYERS)], hq, w.max_blocks_per_seq, w.scale,
-                               max_batch=B, max_context_len=maxctx, buckets=[B])
-    runner.run(qs, ks, vs, slots, ctx, tab)
-    graph = runner.graphs[B]
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    g1.record(stream)
-    torch.cuda.synchronize()
-    graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, device)
-    del runner, graph
 
-    extra = {"decode_step_cuda_graph": {"ms_per_step": round(graph_ms, 4),
-                                        "GB/s": round(step_bytes * world / (graph_ms / 1e3) / 1e9, 2),
-                                        "note": "same 28-layer step replayed from one captured CUDA graph"}}
+    def fused_step():
+        for l in range(LAYERS):
+            pkv.paged_attn_decode_fused_write(qs[l], ks[l], vs[l], slots, kv[0, l], kv[1, l], ctx, tab, w.scale,
+                                              out=outs[l], workspace=ws, max_context_len=maxctx)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+
+    extra = {}
+    for name, fused in (("decode_step_cuda_graph", False), ("decode_step_fused_write_cuda_graph", True)):
+        runner = DecodeGraphRunner([(kv[0, l], kv[1, l]) for l in range(LAYERS)], hq, w.max_blocks_per_seq, w.scale,
+                                   max_batch=B, max_context_len=maxctx, buckets=[B], fused=fused)
+        runner.run(qs, ks, vs, slots, ctx, tab)
+        gms = timed(runner.graphs[B].replay)
+        extra[name] = {"ms_per_step": round(gms, 4), "GB/s": round(step_bytes * world / (gms / 1e3) / 1e9, 2)}
+        del runner
+    fms = timed(fused_step)
+    extra["decode_step_fused_write"] = {"ms_per_step": round(fms, 4),
+                                        "GB/s": round(step_bytes * world / (fms / 1e3) / 1e9, 2)}
     if not args.no_extra:
         extra.update(run_extras(torch, pkv, device, gen, pk))
     assert pkv.device_error() == [], "device error during the benchmark"

@@ -151,6 +151,31 @@ PKV_API int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, co
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Decode attention with the KV-cache write fused in: the same result as
+ * pkv_kv_cache_write(k_new, v_new, slot_mapping, ...) followed by
+ * pkv_paged_attn_decode(...), in one call (page section "第六站：注意力层":
+ * write the step's K/V first, then attend).  Each sequence's new K/V row is
+ * written by the kernel that then reads it, which saves the separate write
+ * launch and its pass over the new rows.
+ *
+ *   k_new, v_new   [batch, num_kv_heads, head_dim] bf16, row b at element
+ *                  b * k_token_stride (resp. v_token_stride); 16-byte aligned.
+ *   slot_mapping   [batch] int32: the slot of position context_lens[b] - 1
+ *                  (the new token), or -1 for a padding row.  A slot that is
+ *                  neither is not written and flags PKV_DEVERR_SLOT_RANGE
+ *                  (writing it could race with the attention's own reads).
+ *   k_cache, v_cache  written at those slots, read as in pkv_paged_attn_decode.
+ * Every other argument is as in pkv_paged_attn_decode.
+ */
+PKV_API int pkv_paged_attn_decode_fused_write(
+    const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride, const pkv_bf16* v_new,
+    int64_t v_token_stride, const int32_t* slot_mapping, pkv_bf16* k_cache, pkv_bf16* v_cache,
+    const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, int32_t max_context_len, float scale, pkv_bf16* out, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/*
  * Varlen causal prefill attention (page sections "第二站" -- every step
  * computes from num_cached_tokens onward; "第三站" -- only the first sequence
  * of a step may be a split chunk; "第六站" -- with prefix hits or a chunk

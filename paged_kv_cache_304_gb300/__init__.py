@@ -77,6 +77,9 @@ def load(path: str | None = None):
         lib.pkv_paged_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp,
                                               vp, sz, vp]
         lib.pkv_paged_attn_decode.restype = ctypes.c_int
+        lib.pkv_paged_attn_decode_fused_write.argtypes = [vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                          i32, i32, i32, i32, f32, vp, vp, sz, vp]
+        lib.pkv_paged_attn_decode_fused_write.restype = ctypes.c_int
         lib.pkv_paged_attn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                                i32, f32, vp, vp]
         lib.pkv_paged_attn_prefill.restype = ctypes.c_int
@@ -175,6 +178,47 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), context_lens.data_ptr(), block_tables.data_ptr(), maxb,
         B, hq, hkv, d, bs, nb, int(max_context_len), float(scale), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(q)))
+    return out
+
+
+def paged_attn_decode_fused_write(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                  slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  context_lens: torch.Tensor, block_tables: torch.Tensor, scale: float,
+                                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                  max_context_len: int | None = None) -> torch.Tensor:
+    """kv_cache_write(k_new, v_new, slot_mapping, ...) + paged_attn_decode(...) in one call.
+
+    slot_mapping[b] must be the slot of position context_lens[b] - 1 or -1.
+    """
+    lib = load()
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev(t, n, torch.bfloat16)
+    for t, n in ((slot_mapping, "slot_mapping"), (context_lens, "context_lens"), (block_tables, "block_tables")):
+        _dev(t, n, torch.int32)
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    B, hq, dq = (int(x) for x in q.shape)
+    if dq != d or not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, Hq, head_dim]")
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if t.shape[0] != B or t[0].numel() != hkv * d or (B and not t[0].is_contiguous()):
+            raise ValueError(f"{name} must be [B, {hkv}, {d}] with contiguous rows")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be contiguous [B, max_blocks]")
+    if context_lens.shape != (B,) or slot_mapping.shape != (B,):
+        raise ValueError("context_lens and slot_mapping must be [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, q.device, d)
+    maxb = int(block_tables.shape[1])
+    if max_context_len is None:
+        max_context_len = maxb * bs
+    _check("pkv_paged_attn_decode_fused_write", lib.pkv_paged_attn_decode_fused_write(
+        q.data_ptr(), k_new.data_ptr(), k_new.stride(0) if B else hkv * d, v_new.data_ptr(),
+        v_new.stride(0) if B else hkv * d, slot_mapping.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        context_lens.data_ptr(), block_tables.data_ptr(), maxb, B, hq, hkv, d, bs, nb, int(max_context_len),
+        float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(q)))
     return out
 
 

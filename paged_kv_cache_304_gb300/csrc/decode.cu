@@ -76,6 +76,14 @@ struct DecodeParams {
   uint32_t kv_tile_bytes;  // kT * Hkv * 256
   uint32_t stage_bytes;    // 2 * kv_tile_bytes
   uint32_t q_slot_bytes;   // Hq * 256 rounded up to 1 KiB
+  // fused KV write (fuse_write != 0): new token rows and their slots
+  const uint4* k_new;
+  const uint4* v_new;
+  int64_t k_stride_vec, v_stride_vec;  // token strides in 16-byte chunks
+  const int32_t* slots;
+  uint4* k_cache_w;
+  uint4* v_cache_w;
+  int32_t fuse_write;
 };
 
 __device__ __forceinline__ int clamp_len(int L, int lmax) {
@@ -131,6 +139,33 @@ __device__ __forceinline__ int load_block(const DecodeParams& p, int b, int lb) 
     phys = 0;
   }
   return phys;
+}
+
+// Fused KV write, by the whole producer warp of the one CTA whose share holds
+// position L-1 of sequence b: copy the new token's K and V rows (all kv heads)
+// to its slot, then make the writes visible to this thread's later TMA reads.
+// The slot must be the slot of position L-1 (the decode invariant); -1 means
+// a padding row (nothing written); any other value is flagged and skipped,
+// since writing elsewhere could race with other CTAs' reads.
+__device__ void write_new_token(const DecodeParams& p, int b, int L, int lane) {
+  const int s = __ldg(p.slots + b);
+  if (s == -1) return;
+  const int pos = L - 1;
+  const int phys = __ldg(p.tables + static_cast<int64_t>(b) * p.maxb + pos / kBlockSize);
+  if (phys < 0 || phys >= p.num_blocks || s != phys * kBlockSize + pos % kBlockSize) {
+    if (lane == 0) atomicOr(&g_err_decode, PKV_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const int row_vecs = p.Hkv * kHeadDim / 8;
+  const uint4* ks = p.k_new + static_cast<int64_t>(b) * p.k_stride_vec;
+  const uint4* vs = p.v_new + static_cast<int64_t>(b) * p.v_stride_vec;
+  uint4* kd = p.k_cache_w + static_cast<int64_t>(s) * row_vecs;
+  uint4* vd = p.v_cache_w + static_cast<int64_t>(s) * row_vecs;
+  for (int c = lane; c < row_vecs; c += 32) {
+    kd[c] = __ldg(ks + c);
+    vd[c] = __ldg(vs + c);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Issue every tile of unit (b, [lo, hi)).  Lane 0 of the producer warp only.
@@ -240,6 +275,8 @@ __device__ void producer(const DecodeParams& p, const Smem& sm, const CUtensorMa
         const int loj = __shfl_sync(0xffffffffu, lo_rel, j);
         const int hij = __shfl_sync(0xffffffffu, hi_rel, j);
         const int Lj = __shfl_sync(0xffffffffu, L, j);
+        if (p.fuse_write && hij == Lj) write_new_token(p, bj, Lj, lane);
+        __syncwarp();
         if (lane == 0 && ps.ok) emit_unit(p, sm, kmap, vmap, ps, bj, loj, hij, Lj, bj + blockIdx.x);
         ps.ok = __shfl_sync(0xffffffffu, ps.ok, 0);
         ps.it = __shfl_sync(0xffffffffu, ps.it, 0);
@@ -547,6 +584,14 @@ cudaError_t launch_paged_attn_decode(const DecodeArgs& a, const CacheMaps& maps,
   p.kv_tile_bytes = static_cast<uint32_t>(kT * a.num_kv_heads * kHeadDim * 2);
   p.stage_bytes = 2 * p.kv_tile_bytes;
   p.q_slot_bytes = static_cast<uint32_t>((a.num_q_heads * kHeadDim * 2 + 1023) & ~1023);
+  p.fuse_write = a.k_new != nullptr;
+  p.k_new = reinterpret_cast<const uint4*>(a.k_new);
+  p.v_new = reinterpret_cast<const uint4*>(a.v_new);
+  p.k_stride_vec = a.k_stride / 8;
+  p.v_stride_vec = a.v_stride / 8;
+  p.slots = a.slot_mapping;
+  p.k_cache_w = reinterpret_cast<uint4*>(a.k_cache);
+  p.v_cache_w = reinterpret_cast<uint4*>(a.v_cache);
   const size_t smem = 1024 + kStages * p.stage_bytes + kQSlots * p.q_slot_bytes +
                       kStages * sizeof(TileHeader) + (2 * kStages + 2 * kQSlots) * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

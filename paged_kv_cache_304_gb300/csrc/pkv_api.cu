@@ -149,11 +149,16 @@ size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t he
   return decode_workspace_bytes(batch, num_q_heads, sms);
 }
 
-int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
-                          const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                          int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
-                          pkv_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the plain and the fused-write decode entry points.
+int decode_common(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache, const int32_t* context_lens,
+                  const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                  int32_t max_context_len, float scale, pkv_bf16* out, void* workspace, size_t workspace_bytes,
+                  void* stream, DecodeArgs& a) {
   if (batch < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
   int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
   if (st != PKV_OK) return st;
@@ -168,7 +173,6 @@ int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_
   CacheMaps maps;
   if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kDecodeTileTokens, num_kv_heads, &maps))
     return PKV_ERR_CUDA;
-  DecodeArgs a;
   a.q = q;
   a.context_lens = context_lens;
   a.block_tables = block_tables;
@@ -183,6 +187,47 @@ int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_
   a.workspace = workspace;
   cudaError_t e = launch_paged_attn_decode(a, maps, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                          const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                          pkv_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  DecodeArgs a;
+  return decode_common(q, k_cache, v_cache, context_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
+                       workspace_bytes, stream, a);
+}
+
+int pkv_paged_attn_decode_fused_write(const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride,
+                                      const pkv_bf16* v_new, int64_t v_token_stride, const int32_t* slot_mapping,
+                                      pkv_bf16* k_cache, pkv_bf16* v_cache, const int32_t* context_lens,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                                      pkv_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (batch > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_NULL;
+    if (k_token_stride < row || v_token_stride < row) return PKV_ERR_SHAPE;
+    if (k_token_stride % 8 || v_token_stride % 8 || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGN;
+  }
+  DecodeArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_stride = k_token_stride;
+  a.v_stride = v_token_stride;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  return decode_common(q, k_cache, v_cache, context_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
+                       workspace_bytes, stream, a);
 }
 
 int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,

@@ -57,6 +57,16 @@ struct DecodeArgs {
   int32_t max_context_len;
   float scale;
   void* workspace;
+  // Fused KV write (optional; all null for plain decode): each sequence's new
+  // token row k_new[b] / v_new[b] (token strides in elements) is written to
+  // k_cache / v_cache at slot_mapping[b] before it is read.
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
+  int64_t k_stride = 0;
+  int64_t v_stride = 0;
+  const int32_t* slot_mapping = nullptr;
+  uint16_t* k_cache = nullptr;
+  uint16_t* v_cache = nullptr;
 };
 // Tensor maps over the caches, built by the front end (see pkv_api.cu).
 // `per_head` selects the layout of the copy: one 5-D box per K (or V) tile,

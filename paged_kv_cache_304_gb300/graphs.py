@@ -27,7 +27,7 @@ from dataclasses import dataclass
 
 import torch
 
-from . import decode_workspace, kv_cache_write, paged_attn_decode
+from . import decode_workspace, kv_cache_write, paged_attn_decode, paged_attn_decode_fused_write
 
 
 def graph_batch_sizes(max_batch: int = 512) -> list[int]:
@@ -57,10 +57,12 @@ class DecodeGraphRunner:
     max_blocks_per_seq: width of the block-table rows.
     max_context_len: host-known bound of the context lengths (captured into
     the graphs, so it must hold for every replay).
+    fused: capture paged_attn_decode_fused_write (write inside the decode
+    kernel) instead of kv_cache_write followed by paged_attn_decode.
     """
 
     def __init__(self, layers, num_q_heads: int, max_blocks_per_seq: int, scale: float,
-                 max_batch: int = 512, max_context_len: int | None = None, buckets=None):
+                 max_batch: int = 512, max_context_len: int | None = None, buckets=None, fused: bool = False):
         if not layers:
             raise ValueError("need at least one layer")
         k0 = layers[0][0]
@@ -71,6 +73,7 @@ class DecodeGraphRunner:
         self.max_batch = max_batch
         self.max_blocks = max_blocks_per_seq
         self.scale = float(scale)
+        self.fused = fused
         self.max_context_len = max_context_len if max_context_len is not None else max_blocks_per_seq * bs
         self.buckets = sorted(buckets or graph_batch_sizes(max_batch))
         nl = len(layers)
@@ -91,6 +94,11 @@ class DecodeGraphRunner:
     def _step(self, b: int) -> None:
         st = self.static
         for li, (kc, vc) in enumerate(self.layers):
+            if self.fused:
+                paged_attn_decode_fused_write(st.q[li, :b], st.k_new[li, :b], st.v_new[li, :b], st.slots[:b], kc, vc,
+                                              st.ctx[:b], st.tables[:b], self.scale, out=st.out[li, :b],
+                                              workspace=self.workspace, max_context_len=self.max_context_len)
+                continue
             kv_cache_write(st.k_new[li, :b], st.v_new[li, :b], st.slots[:b], kc, vc)
             paged_attn_decode(st.q[li, :b], kc, vc, st.ctx[:b], st.tables[:b], self.scale, out=st.out[li, :b],
                               workspace=self.workspace, max_context_len=self.max_context_len)

@@ -23,7 +23,8 @@ def lib():
 
 def test_header_declares_the_three_calls():
     names = pkv.exported_functions()
-    for n in ("pkv_kv_cache_write", "pkv_paged_attn_decode", "pkv_paged_attn_prefill"):
+    for n in ("pkv_kv_cache_write", "pkv_paged_attn_decode", "pkv_paged_attn_prefill",
+              "pkv_paged_attn_decode_fused_write"):
         assert n in names
 
 
