@@ -575,8 +575,30 @@ def _prefill_extra(torch, pkv, device, gen, w: W.PrefillWorkload, pk, reps=10):
             "flops": flops}
 
 
+def _metadata_extra(torch, pkv, device, w, reps=20):
+    """Device-side step metadata (slot mapping, cu_seqlens, packed tables)."""
+    if isinstance(w, W.DecodeWorkload):
+        L = w.context_lens[: w.real_batch].astype(np.int64)
+        c = L - 1
+    else:
+        L = w.seqlens_k.astype(np.int64)
+        c = L - w.seqlens_q
+    tabs = [w.block_tables[i, : -(-int(L[i]) // 256)] for i in range(L.size)]
+    offs = np.zeros(L.size + 1, np.int32)
+    offs[1:] = np.cumsum([t.size for t in tabs])
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    args = (dev(np.concatenate(tabs)), dev(offs), dev(c), dev(L), int((L - c).sum()), w.max_blocks_per_seq,
+            w.num_blocks)
+    ms = _time_calls(torch, lambda: pkv.prepare_metadata(*args), reps)
+    return {"us": round(ms * 1e3, 2), "sequences": int(L.size), "new_tokens": int((L - c).sum())}
+
+
 def run_extras(torch, pkv, device, gen, pk):
     out = {}
+    out["metadata_qwen3_0.6b_decode_b256"] = _metadata_extra(torch, pkv, device, W.qwen3_0p6b_decode(fill_caches=False))
+    out["metadata_chunked_prefill_prefix"] = _metadata_extra(torch, pkv, device,
+                                                             W.chunked_prefill_prefix(fill_caches=False))
+    out["metadata_qwen3_8b_prefill_4x8192"] = _metadata_extra(torch, pkv, device, W.qwen3_8b_prefill(fill_caches=False))
     out["graph_padded_decode_b500_pad512"] = _decode_extra(torch, pkv, device, gen,
                                                             W.graph_padded_decode(fill_caches=False), pk)
     out["qwen3_8b_decode_b64"] = _decode_extra(torch, pkv, device, gen, W.qwen3_8b_decode(fill_caches=False), pk)

@@ -239,6 +239,38 @@ PKV_API int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_c
                                           void* stream);
 
 /*
+ * Step metadata on the device (page section "第五站：执行准备与 KV 容量":
+ * prepare_prefill / prepare_decode build the slot mapping with
+ * slot = block_table[p / block_size] * block_size + p % block_size and feed
+ * only the tokens from num_cached_tokens onward, "第二站"; the varlen attention
+ * calls take cumulative lengths, "第六站").
+ *
+ * Inputs, one entry per sequence i (num_seqs S):
+ *   block_ids, table_offsets [S+1]  sequence i's block table is
+ *                 block_ids[table_offsets[i] .. table_offsets[i+1]-1].
+ *   num_cached [S]   c_i, tokens already in the cache (prefix hits and earlier
+ *                 chunks; L_i - 1 for a decode step).
+ *   seq_lens [S]     L_i, tokens in the cache after this step (c_i < L_i).
+ *   token_capacity   entries of slot_mapping (host-known bound of the new
+ *                 tokens, sum of L_i - c_i; extra entries are set to -1).
+ * Outputs:
+ *   cu_seqlens_q [S+1], cu_seqlens_k [S+1]  prefix sums of L_i - c_i and L_i;
+ *   context_lens [S] = L_i;  slot_mapping [token_capacity]: the slot of each
+ *   new token, sequence by sequence, positions c_i .. L_i-1, then -1;
+ *   block_tables [S, max_blocks_per_seq]: the tables packed, -1 padded.
+ * A sequence whose table is shorter than ceil(L_i / block_size) blocks (the
+ * decode rule: a token at a position that is a multiple of block_size opens a
+ * new block) or whose lengths are inconsistent contributes no tokens and
+ * flags PKV_DEVERR_LEN_RANGE; more tokens than token_capacity also flag it.
+ */
+PKV_API int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets,
+                                 const int32_t* num_cached, const int32_t* seq_lens, int32_t num_seqs,
+                                 int32_t token_capacity, int32_t max_blocks_per_seq, int32_t block_size,
+                                 int32_t num_blocks, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
+                                 int32_t* context_lens, int32_t* slot_mapping, int32_t* block_tables,
+                                 void* stream);
+
+/*
  * Read (and, if `clear` is nonzero, reset) the device error word of the
  * current device.  Synchronises the device.  *out receives an OR of
  * PKV_DEVERR_* bits set by kernels since the last clear.

@@ -83,6 +83,8 @@ def load(path: str | None = None):
         lib.pkv_paged_attn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                                i32, f32, vp, vp]
         lib.pkv_paged_attn_prefill.restype = ctypes.c_int
+        lib.pkv_prepare_metadata.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.pkv_prepare_metadata.restype = ctypes.c_int
         lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         lib.pkv_device_error.restype = ctypes.c_int
         if path is None:
@@ -252,6 +254,41 @@ def paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
         block_tables.data_ptr(), int(block_tables.shape[1]), S, T, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
         bs, nb, float(scale), out.data_ptr(), _stream(q)))
+    return out
+
+
+def prepare_metadata(block_ids: torch.Tensor, table_offsets: torch.Tensor, num_cached: torch.Tensor,
+                     seq_lens: torch.Tensor, token_capacity: int, max_blocks_per_seq: int, num_blocks: int,
+                     block_size: int = 256) -> dict:
+    """Step metadata on the device from per-sequence (block table, num_cached, length).
+
+    block_ids/table_offsets: the block tables as a CSR pair (int32); num_cached,
+    seq_lens: [S] int32.  Returns device tensors cu_seqlens_q, cu_seqlens_k,
+    context_lens, slot_mapping [token_capacity] (-1 past the real tokens) and
+    block_tables [S, max_blocks_per_seq].
+    """
+    lib = load()
+    for t, n in ((block_ids, "block_ids"), (table_offsets, "table_offsets"), (num_cached, "num_cached"),
+                 (seq_lens, "seq_lens")):
+        _dev(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    S = int(seq_lens.shape[0])
+    if num_cached.shape != (S,) or table_offsets.shape != (S + 1,):
+        raise ValueError("num_cached must be [S] and table_offsets [S+1]")
+    dev = seq_lens.device
+    out = {
+        "cu_seqlens_q": torch.empty(S + 1, dtype=torch.int32, device=dev),
+        "cu_seqlens_k": torch.empty(S + 1, dtype=torch.int32, device=dev),
+        "context_lens": torch.empty(S, dtype=torch.int32, device=dev),
+        "slot_mapping": torch.empty(max(token_capacity, 0), dtype=torch.int32, device=dev),
+        "block_tables": torch.empty((S, max_blocks_per_seq), dtype=torch.int32, device=dev),
+    }
+    _check("pkv_prepare_metadata", lib.pkv_prepare_metadata(
+        block_ids.data_ptr(), table_offsets.data_ptr(), num_cached.data_ptr(), seq_lens.data_ptr(), S,
+        int(token_capacity), int(max_blocks_per_seq), int(block_size), int(num_blocks),
+        out["cu_seqlens_q"].data_ptr(), out["cu_seqlens_k"].data_ptr(), out["context_lens"].data_ptr(),
+        out["slot_mapping"].data_ptr(), out["block_tables"].data_ptr(), _stream(seq_lens)))
     return out
 
 

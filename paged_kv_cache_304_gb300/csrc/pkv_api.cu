@@ -343,14 +343,48 @@ int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, co
                                out, scratch, PKV_DECODE_STATIC_SCRATCH_BYTES, stream);
 }
 
+int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets, const int32_t* num_cached,
+                         const int32_t* seq_lens, int32_t num_seqs, int32_t token_capacity,
+                         int32_t max_blocks_per_seq, int32_t block_size, int32_t num_blocks, int32_t* cu_seqlens_q,
+                         int32_t* cu_seqlens_k, int32_t* context_lens, int32_t* slot_mapping, int32_t* block_tables,
+                         void* stream) {
+  if (num_seqs < 0 || token_capacity < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * block_size >= (int64_t{1} << 31)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!block_ids || !table_offsets || !num_cached || !seq_lens || !cu_seqlens_q || !cu_seqlens_k || !context_lens ||
+      !block_tables || (token_capacity > 0 && !slot_mapping))
+    return PKV_ERR_NULL;
+  const int sms = sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  MetaArgs a;
+  a.block_ids = block_ids;
+  a.table_offsets = table_offsets;
+  a.num_cached = num_cached;
+  a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs;
+  a.token_capacity = token_capacity;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.context_lens = context_lens;
+  a.slot_mapping = slot_mapping;
+  a.block_tables = block_tables;
+  cudaError_t e = launch_prepare_metadata(a, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int pkv_device_error(uint32_t* out, int clear) {
   if (!out) return PKV_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0;
   if (read_error_kv_write(&a, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (read_error_decode(&b, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (read_error_prefill(&c, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
-  *out = a | b | c;
+  if (read_error_metadata(&d, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
+  *out = a | b | c | d;
   return PKV_OK;
 }
 

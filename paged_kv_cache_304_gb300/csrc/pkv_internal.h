@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <algorithm>
 #include <utility>
 
 #include "pkv.h"
@@ -101,9 +102,25 @@ struct PrefillArgs {
 cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv_maps,
                                       const CUtensorMap& q_map, int num_sms, cudaStream_t stream);
 
+// ---- step metadata
+struct MetaArgs {
+  const int32_t* block_ids;
+  const int32_t* table_offsets;
+  const int32_t* num_cached;
+  const int32_t* seq_lens;
+  int32_t num_seqs, token_capacity, max_blocks_per_seq, block_size, num_blocks;
+  int32_t* cu_seqlens_q;
+  int32_t* cu_seqlens_k;
+  int32_t* context_lens;
+  int32_t* slot_mapping;
+  int32_t* block_tables;
+};
+cudaError_t launch_prepare_metadata(const MetaArgs& a, int num_sms, cudaStream_t stream);
+
 // ---- device error words (one per translation unit)
 cudaError_t read_error_kv_write(uint32_t* out, bool clear);
 cudaError_t read_error_decode(uint32_t* out, bool clear);
 cudaError_t read_error_prefill(uint32_t* out, bool clear);
+cudaError_t read_error_metadata(uint32_t* out, bool clear);
 
 }  // namespace pkv
