@@ -593,8 +593,23 @@ def _metadata_extra(torch, pkv, device, w, reps=20):
     return {"us": round(ms * 1e3, 2), "sequences": int(L.size), "new_tokens": int((L - c).sum())}
 
 
+def _sampler_extra(torch, pkv, device, gen, pk, B=256, V=151936, reps=20):
+    """Exponential-race sampling over a Qwen3-sized vocabulary (4 bytes of
+    fp32 logits per token read once)."""
+    logits = torch.randn((B, V), generator=gen, device=device, dtype=torch.float32) * 2
+    temps = torch.full((B,), 0.7, device=device, dtype=torch.float32)
+    out = torch.empty(B, dtype=torch.int32, device=device)
+    ws = torch.empty(max(256, int(pkv.load().pkv_sample_workspace_bytes(B, V))), dtype=torch.uint8, device=device)
+    ms = _time_calls(torch, lambda: pkv.sample_exponential_race(logits, temps, 1, 2, out=out, workspace=ws), reps)
+    nbytes = B * V * 4 + B * 8
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "batch": B, "vocab": V}
+
+
 def run_extras(torch, pkv, device, gen, pk):
     out = {}
+    out["sampler_b256_vocab151936"] = _sampler_extra(torch, pkv, device, gen, pk)
     out["metadata_qwen3_0.6b_decode_b256"] = _metadata_extra(torch, pkv, device, W.qwen3_0p6b_decode(fill_caches=False))
     out["metadata_chunked_prefill_prefix"] = _metadata_extra(torch, pkv, device,
                                                              W.chunked_prefill_prefix(fill_caches=False))

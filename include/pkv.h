@@ -271,6 +271,32 @@ PKV_API int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_
                                  void* stream);
 
 /*
+ * Exponential-race sampling of the next token (page section "其余部分":
+ * temperature-only sampling that divides the probabilities by exponentially
+ * distributed random numbers and takes the largest quotient -- equivalent to
+ * sampling by probability; temperature 0 is not allowed).
+ *
+ *   logits        [batch, vocab] float32, row b at element b * row_stride.
+ *   temperatures  [batch] float32, each finite and > 0 (otherwise that row's
+ *                 token is -1 and PKV_DEVERR_LEN_RANGE is set).
+ *   seed, offset  select the random numbers: token i of row b uses output word
+ *                 i % 4 of Philox4x32-10 (counter {i/4, b, offset_lo,
+ *                 offset_hi}, key {seed_lo, seed_hi}; Salmon et al., SC 2011)
+ *                 as U = ((word >> 8) + 0.5) / 2^24, E = -ln U.  Use a new
+ *                 offset (or seed) for every step.
+ *   out_tokens    [batch] int32: argmax_i softmax(logits / T)_i / E_i (ties go
+ *                 to the smaller index; computed as the argmax of
+ *                 l_i log2(e) / T - log2(-log2 U_i)).
+ *   workspace     >= pkv_sample_workspace_bytes(batch, vocab) bytes, 256-byte
+ *                 aligned, need not be initialised.
+ */
+PKV_API size_t pkv_sample_workspace_bytes(int32_t batch, int32_t vocab);
+PKV_API int pkv_sample_exponential_race(const float* logits, int64_t row_stride, const float* temperatures,
+                                        int32_t batch, int32_t vocab, uint64_t seed, uint64_t offset,
+                                        int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
+/*
  * Read (and, if `clear` is nonzero, reset) the device error word of the
  * current device.  Synchronises the device.  *out receives an OR of
  * PKV_DEVERR_* bits set by kernels since the last clear.

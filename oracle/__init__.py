@@ -81,6 +81,12 @@ class Oracle:
         lib.pkv_oracle_paged_attn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
                                                       ctypes.c_double, vp, i64, vp]
         lib.pkv_oracle_paged_attn_prefill.restype = ctypes.c_int
+        lib.pkv_oracle_philox4x32_10.argtypes = [vp, vp, vp]
+        lib.pkv_oracle_philox4x32_10.restype = None
+        lib.pkv_oracle_uniform.argtypes = [i64, i64, ctypes.c_uint64, ctypes.c_uint64]
+        lib.pkv_oracle_uniform.restype = ctypes.c_double
+        lib.pkv_oracle_sample.argtypes = [vp, i64, vp, i64, i64, ctypes.c_uint64, ctypes.c_uint64, vp, vp]
+        lib.pkv_oracle_sample.restype = ctypes.c_int
         lib.pkv_oracle_num_threads.restype = ctypes.c_int
         lib.pkv_oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = lib
@@ -154,6 +160,31 @@ class Oracle:
                                                       nb, float(scale), rp, nr, _ptr(out)),
                "paged_attn_prefill")
         return out
+
+
+    def philox4x32_10(self, counter, key) -> list[int]:
+        """Philox4x32-10 block: four 32-bit words for a 4-word counter and 2-word key."""
+        c = np.ascontiguousarray(counter, dtype=np.uint32)
+        k = np.ascontiguousarray(key, dtype=np.uint32)
+        out = np.zeros(4, dtype=np.uint32)
+        self.lib.pkv_oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+        return [int(x) for x in out]
+
+    def uniform(self, b: int, i: int, seed: int, offset: int) -> float:
+        return float(self.lib.pkv_oracle_uniform(b, i, seed, offset))
+
+    def sample(self, logits, temperatures, seed: int, offset: int = 0, with_scores: bool = False):
+        """Exponential-race sampling in fp64.  logits float32 [B, V].
+
+        Returns tokens int32 [B] (and float64 scores [B, V] = log p - log E)."""
+        lg = _c(logits, np.float32)
+        B, V = lg.shape
+        t = _c(temperatures, np.float32)
+        tokens = np.empty(B, dtype=np.int32)
+        scores = np.empty((B, V), dtype=np.float64) if with_scores else None
+        _check(self.lib.pkv_oracle_sample(_ptr(lg), V, _ptr(t), B, V, seed, offset, _ptr(tokens),
+                                          _ptr(scores) if with_scores else None), "sample")
+        return (tokens, scores) if with_scores else tokens
 
 
 def default() -> Oracle:

@@ -241,3 +241,103 @@ int pkv_oracle_paged_attn_prefill(const uint16_t* q, const uint16_t* k_cache, co
   }
   return err;
 }
+
+/*
+ * Exponential-race sampler (page section "其余部分": temperature-only
+ * sampling; the probabilities are divided by exponentially distributed
+ * random numbers and the largest quotient wins, which samples each token with
+ * its probability; temperature 0 is not allowed).
+ *
+ * Random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+ * Numbers: As Easy as 1, 2, 3", SC 2011), a counter-based generator.  For row
+ * b and token i the 32-bit word is output word (i % 4) of
+ * Philox(counter = {i / 4, b, offset_lo, offset_hi}, key = {seed_lo, seed_hi});
+ * U = (word >> 8) + 0.5) / 2^24 lies strictly inside (0, 1) and
+ * E = -ln(U) ~ Exp(1).
+ *
+ * Steps, per row, in double: p = softmax(logits / T) (maximum subtracted),
+ * E_i from the generator, token = the first i maximising p_i / E_i.
+ * T must be finite and > 0; otherwise the row's token is -1.
+ */
+static uint32_t mulhi32(uint32_t a, uint32_t b) { return (uint32_t)(((uint64_t)a * b) >> 32); }
+
+void pkv_oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint32_t k[2] = {key_in[0], key_in[1]};
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k[0] += 0x9E3779B9u;
+      k[1] += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = mulhi32(0xD2511F53u, c[0]), lo0 = 0xD2511F53u * c[0];
+    const uint32_t hi1 = mulhi32(0xCD9E8D57u, c[2]), lo1 = 0xCD9E8D57u * c[2];
+    const uint32_t n0 = hi1 ^ c[1] ^ k[0], n1 = lo1, n2 = hi0 ^ c[3] ^ k[1], n3 = lo0;
+    c[0] = n0;
+    c[1] = n1;
+    c[2] = n2;
+    c[3] = n3;
+  }
+  out[0] = c[0];
+  out[1] = c[1];
+  out[2] = c[2];
+  out[3] = c[3];
+}
+
+/* The uniform U in (0, 1) of row b, token i. */
+double pkv_oracle_uniform(int64_t b, int64_t i, uint64_t seed, uint64_t offset) {
+  const uint32_t ctr[4] = {(uint32_t)(i / 4), (uint32_t)b, (uint32_t)offset, (uint32_t)(offset >> 32)};
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t w[4];
+  pkv_oracle_philox4x32_10(ctr, key, w);
+  return ((double)(w[i % 4] >> 8) + 0.5) / 16777216.0;
+}
+
+/*
+ * logits [batch, vocab] float32 (row stride in elements), temperatures
+ * [batch]; writes tokens [batch] and, if `scores` is not NULL, the log-space
+ * score log(p_i) - log(E_i) of every token (for near-tie checks).
+ */
+int pkv_oracle_sample(const float* logits, int64_t row_stride, const float* temperatures, int64_t batch,
+                      int64_t vocab, uint64_t seed, uint64_t offset, int32_t* tokens, double* scores) {
+  if (batch < 0 || vocab <= 0 || row_stride < vocab) return ORACLE_ERR_ARG;
+  int err = ORACLE_OK;
+#pragma omp parallel
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)vocab);
+    if (!p) {
+#pragma omp atomic write
+      err = ORACLE_ERR_NOMEM;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t b = 0; b < batch; ++b) {
+      const double T = temperatures[b];
+      if (!p || !(T > 0.0) || !isfinite(T)) {
+        tokens[b] = -1;
+        continue;
+      }
+      const float* l = logits + b * row_stride;
+      double m = -INFINITY;
+      for (int64_t i = 0; i < vocab; ++i)
+        if ((double)l[i] / T > m) m = (double)l[i] / T;
+      double sum = 0.0;
+      for (int64_t i = 0; i < vocab; ++i) {
+        p[i] = exp((double)l[i] / T - m);
+        sum += p[i];
+      }
+      int64_t best = 0;
+      double best_q = -1.0;
+      for (int64_t i = 0; i < vocab; ++i) {
+        const double E = -log(pkv_oracle_uniform(b, i, seed, offset));
+        const double q = (p[i] / sum) / E;
+        if (q > best_q) {
+          best_q = q;
+          best = i;
+        }
+        if (scores) scores[b * vocab + i] = log(p[i] / sum) - log(E);
+      }
+      tokens[b] = (int32_t)best;
+    }
+    free(p);
+  }
+  return err;
+}

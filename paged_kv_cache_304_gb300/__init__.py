@@ -85,6 +85,11 @@ def load(path: str | None = None):
         lib.pkv_paged_attn_prefill.restype = ctypes.c_int
         lib.pkv_prepare_metadata.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.pkv_prepare_metadata.restype = ctypes.c_int
+        lib.pkv_sample_workspace_bytes.argtypes = [i32, i32]
+        lib.pkv_sample_workspace_bytes.restype = sz
+        lib.pkv_sample_exponential_race.argtypes = [vp, i64, vp, i32, i32, ctypes.c_uint64, ctypes.c_uint64, vp, vp,
+                                                    sz, vp]
+        lib.pkv_sample_exponential_race.restype = ctypes.c_int
         lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         lib.pkv_device_error.restype = ctypes.c_int
         if path is None:
@@ -289,6 +294,33 @@ def prepare_metadata(block_ids: torch.Tensor, table_offsets: torch.Tensor, num_c
         int(token_capacity), int(max_blocks_per_seq), int(block_size), int(num_blocks),
         out["cu_seqlens_q"].data_ptr(), out["cu_seqlens_k"].data_ptr(), out["context_lens"].data_ptr(),
         out["slot_mapping"].data_ptr(), out["block_tables"].data_ptr(), _stream(seq_lens)))
+    return out
+
+
+def sample_exponential_race(logits: torch.Tensor, temperatures: torch.Tensor, seed: int, offset: int = 0,
+                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Next token per row: argmax softmax(logits / T) / Exp(1) noise (Philox, seed/offset).
+
+    logits [B, V] float32 with contiguous rows; temperatures [B] float32 > 0.
+    Returns int32 [B].
+    """
+    lib = load()
+    _dev(logits, "logits", torch.float32)
+    _dev(temperatures, "temperatures", torch.float32)
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [B, V] with contiguous rows")
+    B, V = (int(x) for x in logits.shape)
+    if temperatures.shape != (B,) or not temperatures.is_contiguous():
+        raise ValueError("temperatures must be contiguous [B]")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    if workspace is None:
+        workspace = torch.empty(max(256, int(lib.pkv_sample_workspace_bytes(B, V))), dtype=torch.uint8,
+                                device=logits.device)
+    _check("pkv_sample_exponential_race", lib.pkv_sample_exponential_race(
+        logits.data_ptr(), logits.stride(0), temperatures.data_ptr(), B, V, int(seed) & (2**64 - 1),
+        int(offset) & (2**64 - 1), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(logits)))
     return out
 
 

@@ -376,6 +376,34 @@ int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets,
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+size_t pkv_sample_workspace_bytes(int32_t batch, int32_t vocab) {
+  if (batch < 0 || vocab <= 0) return 0;
+  return sample_workspace_bytes(batch, vocab);
+}
+
+int pkv_sample_exponential_race(const float* logits, int64_t row_stride, const float* temperatures, int32_t batch,
+                                int32_t vocab, uint64_t seed, uint64_t offset, int32_t* out_tokens, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (batch < 0 || vocab <= 0 || row_stride < vocab) return PKV_ERR_SHAPE;
+  if (batch == 0) return PKV_OK;
+  if (static_cast<int64_t>(batch) * ((vocab + 4095) / 4096) >= (int64_t{1} << 31)) return PKV_ERR_UNSUPPORTED;
+  if (!logits || !temperatures || !out_tokens) return PKV_ERR_NULL;
+  if (!workspace || workspace_bytes < sample_workspace_bytes(batch, vocab)) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGN;
+  SampleArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.temperatures = temperatures;
+  a.batch = batch;
+  a.vocab = vocab;
+  a.seed = seed;
+  a.offset = offset;
+  a.out = out_tokens;
+  a.workspace = workspace;
+  cudaError_t e = launch_sample(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int pkv_device_error(uint32_t* out, int clear) {
   if (!out) return PKV_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
@@ -384,7 +412,9 @@ int pkv_device_error(uint32_t* out, int clear) {
   if (read_error_decode(&b, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (read_error_prefill(&c, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (read_error_metadata(&d, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
-  *out = a | b | c | d;
+  uint32_t e5 = 0;
+  if (read_error_sampler(&e5, clear != 0) != cudaSuccess) return PKV_ERR_CUDA;
+  *out = a | b | c | d | e5;
   return PKV_OK;
 }
 

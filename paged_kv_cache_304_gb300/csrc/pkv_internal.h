@@ -117,10 +117,24 @@ struct MetaArgs {
 };
 cudaError_t launch_prepare_metadata(const MetaArgs& a, int num_sms, cudaStream_t stream);
 
+// ---- exponential-race sampler
+struct SampleArgs {
+  const float* logits;
+  int64_t row_stride;
+  const float* temperatures;
+  int32_t batch, vocab;
+  uint64_t seed, offset;
+  int32_t* out;
+  void* workspace;
+};
+size_t sample_workspace_bytes(int batch, int vocab);
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream);
+
 // ---- device error words (one per translation unit)
 cudaError_t read_error_kv_write(uint32_t* out, bool clear);
 cudaError_t read_error_decode(uint32_t* out, bool clear);
 cudaError_t read_error_prefill(uint32_t* out, bool clear);
 cudaError_t read_error_metadata(uint32_t* out, bool clear);
+cudaError_t read_error_sampler(uint32_t* out, bool clear);
 
 }  // namespace pkv

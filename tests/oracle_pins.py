@@ -382,8 +382,41 @@ def pin_pad_rows(orc):
     assert (out[0] == 0).all() and (out[2] == 0).all() and np.abs(out[1]).sum() > 0
 
 
+# --------------------------------------------------------------------------
+# Exponential-race sampler
+# --------------------------------------------------------------------------
+
+def pin_philox_known_answer(orc):
+    """Philox4x32-10 of the zero counter under the zero key: the published
+    known answer of the generator."""
+    assert orc.philox4x32_10([0, 0, 0, 0], [0, 0]) == [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+
+
+def pin_race_distribution(orc):
+    """The race winner is distributed as softmax(logits / T) (chi-square,
+    60000 independent rows, p-value > 1e-4)."""
+    from scipy.stats import chisquare
+    V, B, T = 8, 60000, 0.7
+    base = np.array([1.0, 0.5, -0.3, 2.0, 0.0, -1.0, 1.5, 0.2], np.float32)
+    tok = orc.sample(np.tile(base, (B, 1)), np.full(B, T, np.float32), seed=99, offset=0)
+    z = base.astype(np.float64) / T
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    counts = np.bincount(tok, minlength=V)
+    assert chisquare(counts, p * counts.sum()).pvalue > 1e-4
+
+
+def pin_low_temperature_is_argmax(orc):
+    """As T -> 0 the race always picks the largest logit."""
+    rng = np.random.default_rng(0)
+    logits = rng.standard_normal((40, 500)).astype(np.float32)
+    tok = orc.sample(logits, np.full(40, 1e-3, np.float32), seed=5, offset=3)
+    assert (tok == logits.argmax(axis=1)).all()
+
+
 ALL_PINS = [
     pin_write_scatter, pin_write_all_padding, pin_single_key, pin_zero_query, pin_equal_keys,
     pin_two_keys_logistic, pin_dominant_key, pin_shift_invariance, pin_sdpa_prefill, pin_sdpa_decode, pin_block_permutation,
     pin_chunk_consistency, pin_causality, pin_shared_prefix, pin_stale_ignored, pin_pad_rows,
+    pin_philox_known_answer, pin_race_distribution, pin_low_temperature_is_argmax,
 ]

@@ -35,6 +35,10 @@ MUTANTS = {
                        "v_cache[s * row_elems + e] = k[i * k_token_stride + e];"),
     "write_ignores_stride": ("k_cache[s * row_elems + e] = k[i * k_token_stride + e];",
                              "k_cache[s * row_elems + e] = k[i * row_elems + e];"),
+    "philox_nine_rounds": ("for (int r = 0; r < 10; ++r) {", "for (int r = 0; r < 9; ++r) {"),
+    "philox_wrong_weyl": ("k[0] += 0x9E3779B9u;", "k[0] += 0x9E3779B8u;"),
+    "sampler_no_temperature": ("p[i] = exp((double)l[i] / T - m);", "p[i] = exp((double)l[i] - m);"),
+    "sampler_times_noise": ("const double q = (p[i] / sum) / E;", "const double q = (p[i] / sum) * E;"),
     "dot_wrong_index": ("widen_bf16(qrow[d]) * widen_bf16(k_cache[base + d]);",
                         "widen_bf16(qrow[d]) * widen_bf16(k_cache[base + (d + 1) % hd]);"),
 }
