@@ -628,7 +628,8 @@ def run_extras(torch, pkv, device, gen, pk):
     return out
 
 
-CASES = ("step", "prefill_8b", "prefill_chunked", "decode_8b", "decode_padded", "decode_tiny", "write_32768")
+CASES = ("step", "prefill_8b", "prefill_chunked", "decode_8b", "decode_padded", "decode_tiny", "write_32768",
+         "sampler")
 
 
 def run_case(args, local):
@@ -661,6 +662,11 @@ def run_case(args, local):
     elif args.case == "decode_tiny":
         w = W.tiny_decode(fill_caches=False)
         res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)
+    elif args.case == "sampler":
+        res = _sampler_extra(torch, pkv, device, gen, pk, reps=reps)
+        print(json.dumps({"case": args.case, "workload": "sampler_b256_vocab151936", "peak_kind": peak_kind, **res}),
+              flush=True)
+        return 0
     else:
         w = W.qwen3_8b_prefill(fill_caches=False)
         res = _write_extra(torch, pkv, device, gen, w, pk, reps=reps)
