@@ -7,10 +7,10 @@
 //
 // The work is a pure copy, bound by HBM: per token, 2 x row_bytes read and
 // 2 x row_bytes written (row_bytes = num_kv_heads * head_dim * 2 = 2 KiB for
-// 8 kv heads of 128).  Each thread moves one 16-byte chunk of K and the
-// matching chunk of V per iteration with 128-bit loads (read-once, no L1
-// allocation) and 128-bit stores, so a warp covers 512 contiguous bytes of a
-// row.  The grid is a multiple of the SM count and strides over all chunks.
+// 8 kv heads of 128).  One warp moves one token row: 128-bit loads (read-once,
+// no L1 allocation) of up to four chunks of K and four of V per lane are all
+// issued before the 128-bit stores, so each SM keeps many loads in flight.
+// The grid is a multiple of the SM count and strides over the tokens.
 #include <cuda_runtime.h>
 
 #include "pkv_device.cuh"
@@ -29,8 +29,10 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return r;
 }
 
-// One 16-byte chunk of K and of V per (token, chunk) pair.  `row_vecs` chunks
-// make one token row; strides are in 16-byte chunks.
+// One warp per token row (grid-strided over tokens): the slot is read once
+// per warp, then each lane loads its 16-byte chunks of the K row and of the V
+// row -- up to four of each, all in flight together -- before storing them.
+// Strides are in 16-byte chunks; `row_vecs` chunks make one row.
 __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__ k, int64_t k_stride,
                                                        const uint4* __restrict__ v, int64_t v_stride,
                                                        const int32_t* __restrict__ slots,
@@ -39,23 +41,39 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
                                                        int32_t row_vecs) {
   griddep_wait();
   griddep_launch_dependents();
-  // num_tokens * row_vecs < 2^31 is checked by the launcher, so 32-bit
-  // index arithmetic (cheap unsigned division) is exact here.
-  const uint32_t total = static_cast<uint32_t>(num_tokens) * static_cast<uint32_t>(row_vecs);
-  const uint32_t step = gridDim.x * blockDim.x;
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += step) {
-    const uint32_t t = i / static_cast<uint32_t>(row_vecs);
-    const uint32_t c = i - t * static_cast<uint32_t>(row_vecs);
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < num_tokens;
+       t += warps) {
     const int64_t s = __ldg(slots + t);
     if (s == -1) continue;
     if (s < 0 || s >= num_slots) {
-      if (c == 0) atomicOr(&g_err_kv_write, PKV_DEVERR_SLOT_RANGE);
+      if (lane == 0) atomicOr(&g_err_kv_write, PKV_DEVERR_SLOT_RANGE);
       continue;
     }
-    const uint4 kv = ld_stream(k + static_cast<int64_t>(t) * k_stride + c);
-    const uint4 vv = ld_stream(v + static_cast<int64_t>(t) * v_stride + c);
-    k_cache[s * row_vecs + c] = kv;
-    v_cache[s * row_vecs + c] = vv;
+    const uint4* ks = k + t * k_stride;
+    const uint4* vs = v + t * v_stride;
+    uint4* kd = k_cache + s * row_vecs;
+    uint4* vd = v_cache + s * row_vecs;
+    for (int c0 = 0; c0 < row_vecs; c0 += 128) {
+      uint4 kr[4], vr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < row_vecs) {
+          kr[u] = ld_stream(ks + c);
+          vr[u] = ld_stream(vs + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < row_vecs) {
+          kd[c] = kr[u];
+          vd[c] = vr[u];
+        }
+      }
+    }
   }
 }
 
@@ -72,10 +90,8 @@ cudaError_t launch_kv_cache_write(const uint16_t* k, int64_t k_stride, const uin
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int threads = 256;
-  const int64_t chunks = static_cast<int64_t>(num_tokens) * row_vecs;
-  if (chunks >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
-  int64_t blocks = (chunks + threads - 1) / threads;
+  const int threads = 256;  // 8 warps = 8 token rows per block and iteration
+  int64_t blocks = (static_cast<int64_t>(num_tokens) + 7) / 8;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread blocks per SM
   if (blocks > cap) blocks = cap;
   return launch_pdl(kv_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,

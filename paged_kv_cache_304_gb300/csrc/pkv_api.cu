@@ -134,7 +134,6 @@ int pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16
   if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
   const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
-  if (static_cast<int64_t>(num_tokens) * (row / 8) >= (int64_t{1} << 31)) return PKV_ERR_UNSUPPORTED;
   cudaError_t e = launch_kv_cache_write(k, k_token_stride, v, v_token_stride, slot_mapping, num_tokens, k_cache,
                                         v_cache, num_slots, static_cast<int32_t>(row),
                                         static_cast<cudaStream_t>(stream));
