@@ -282,7 +282,7 @@ PKV_API int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_
  *   seed, offset  select the random numbers: token i of row b uses output word
  *                 i % 4 of Philox4x32-10 (counter {i/4, b, offset_lo,
  *                 offset_hi}, key {seed_lo, seed_hi}; Salmon et al., SC 2011)
- *                 as U = ((word >> 8) + 0.5) / 2^24, E = -ln U.  Use a new
+ *                 as U = ((word >> 9) + 0.5) / 2^23, E = -ln U.  Use a new
  *                 offset (or seed) for every step.
  *   out_tokens    [batch] int32: argmax_i softmax(logits / T)_i / E_i (ties go
  *                 to the smaller index; computed as the argmax of

@@ -252,7 +252,7 @@ int pkv_oracle_paged_attn_prefill(const uint16_t* q, const uint16_t* k_cache, co
  * Numbers: As Easy as 1, 2, 3", SC 2011), a counter-based generator.  For row
  * b and token i the 32-bit word is output word (i % 4) of
  * Philox(counter = {i / 4, b, offset_lo, offset_hi}, key = {seed_lo, seed_hi});
- * U = (word >> 8) + 0.5) / 2^24 lies strictly inside (0, 1) and
+ * U = ((word >> 9) + 0.5) / 2^23 lies strictly inside (0, 1) and
  * E = -ln(U) ~ Exp(1).
  *
  * Steps, per row, in double: p = softmax(logits / T) (maximum subtracted),
@@ -289,7 +289,7 @@ double pkv_oracle_uniform(int64_t b, int64_t i, uint64_t seed, uint64_t offset) 
   const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
   uint32_t w[4];
   pkv_oracle_philox4x32_10(ctr, key, w);
-  return ((double)(w[i % 4] >> 8) + 0.5) / 16777216.0;
+  return ((double)(w[i % 4] >> 9) + 0.5) / 8388608.0;
 }
 
 /*

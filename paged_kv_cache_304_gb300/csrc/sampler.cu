@@ -14,7 +14,7 @@
 // Random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
 // Numbers: As Easy as 1, 2, 3", SC 2011).  Token i of row b uses output word
 // i % 4 of Philox(counter = {i / 4, b, offset_lo, offset_hi},
-// key = {seed_lo, seed_hi}); U = ((word >> 8) + 0.5) / 2^24 in (0, 1).
+// key = {seed_lo, seed_hi}); U = ((word >> 9) + 0.5) / 2^23 in (0, 1).
 //
 // Kernels: a grid of (4096-token chunk, row) CTAs streams the logits with
 // 16-byte loads, generates the noise in registers and reduces (key, index) to
@@ -66,10 +66,21 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
-// Race key of one token: l * log2(e) / T - log2(-log2(U)).
+// Race key of one token: l * log2(e) / T - log2(-log2(U)), with
+// U = ((word >> 9) + 0.5) / 2^23 built from the float with exponent 0 and the
+// top 23 bits of the word as mantissa ([1, 2)), minus 1 - 2^-24 (exact).
 __device__ __forceinline__ float race_key(float l, float scale, uint32_t word) {
-  const float u = (static_cast<float>(word >> 8) + 0.5f) * 5.9604644775390625e-8f;  // 2^-24
+  const float u = __uint_as_float(0x3F800000u | (word >> 9)) - 0.99999994039535522f;
   return l * scale - fast_log2(-fast_log2(u));
+}
+
+// Within one thread tokens arrive in increasing index order, so a later token
+// replaces the current best only if its key is strictly larger.
+__device__ __forceinline__ void better_in_order(float& bk, int& bi, float k, int i) {
+  if (k > bk) {
+    bk = k;
+    bi = i;
+  }
 }
 
 __device__ __forceinline__ void better(float& bk, int& bi, float k, int i) {
@@ -100,15 +111,15 @@ __global__ void __launch_bounds__(kThreads) sample_chunk_kernel(const SamplePara
                                     p.seed_lo, p.seed_hi);
       if (p.vec4 && i + 3 < p.V) {
         const float4 l = __ldg(reinterpret_cast<const float4*>(row + i));
-        better(bk, bi, race_key(l.x, scale, w.x), i);
-        better(bk, bi, race_key(l.y, scale, w.y), i + 1);
-        better(bk, bi, race_key(l.z, scale, w.z), i + 2);
-        better(bk, bi, race_key(l.w, scale, w.w), i + 3);
+        better_in_order(bk, bi, race_key(l.x, scale, w.x), i);
+        better_in_order(bk, bi, race_key(l.y, scale, w.y), i + 1);
+        better_in_order(bk, bi, race_key(l.z, scale, w.z), i + 2);
+        better_in_order(bk, bi, race_key(l.w, scale, w.w), i + 3);
       } else {
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (i + q < p.V) better(bk, bi, race_key(__ldg(row + i + q), scale, ws[q]), i + q);
+          if (i + q < p.V) better_in_order(bk, bi, race_key(__ldg(row + i + q), scale, ws[q]), i + q);
       }
     }
   }
