@@ -323,9 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = s[u];
 #pragma unroll
-      for (int x = 8; x < 128; ++x) mx[x & 7] = fmaxf(mx[x & 7], s[x]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int x = 8; x < 128; x += 2) mx[(x >> 1) & 7] = fmax3(mx[(x >> 1) & 7], s[x], s[x + 1]);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m_ref, mt * p.sl2);
       float alpha = 1.f;
       if (m_new > m_ref + 8.f) {
@@ -336,16 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // p = 2^(s * scale * log2e - m), packed to bf16 pairs and written over
       // S 32 keys at a time: keys 32q..32q+31 go to columns 16q..16q+15, which
       // hold scores already in registers.
-      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sl2 = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          const float e0 = fast_exp2(fmaf(s[32 * q + x], p.sl2, -mu));
-          const float e1 = fast_exp2(fmaf(s[32 * q + x + 1], p.sl2, -mu));
-          rs[(x >> 1) & 7] += e0 + e1;
-          pk[x >> 1] = pack_bf16x2(e0, e1);
+          const float2 a = ffma2(make_float2(s[32 * q + x], s[32 * q + x + 1]), sl2, nmu);
+          const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+          rs[(x >> 1) & 3] = fadd2(rs[(x >> 1) & 3], e);
+          pk[x >> 1] = pack_bf16x2(e.x, e.y);
         }
         tc::st16u(s_addr + 16 * q, pk);
       }
@@ -361,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::st32(o_addr + cc * 32, o);
         }
       }
-      l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
+      const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+      const float2 rt = fadd2(r01, r23);
+      l = l * alpha + (rt.x + rt.y);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
