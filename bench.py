@@ -2,10 +2,11 @@
 """Benchmark of the paged-KV attention path on GB300.
 
 One step = one Qwen3-0.6B-shaped decode step of every decoder layer: for each
-of 28 layers, write the 256 new tokens' K/V into that layer's paged cache
-(kv_cache_write) and run decode attention over batch 256 with context
-lengths uniform in [100, 2048] (paged_attn_decode); 16 query / 8 kv heads,
-head_dim 128, block_size 256, shuffled block tables.  Inputs are synthetic
+of 28 layers, write the 256 new tokens' K/V into that layer's paged cache and
+run decode attention over batch 256 with context lengths uniform in
+[100, 2048], in one call (paged_attn_decode_fused_write; the separate
+kv_cache_write + paged_attn_decode step is reported too); 16 query / 8 kv
+heads, head_dim 128, block_size 256, shuffled block tables.  Inputs are synthetic
 and seeded (seed 3042); every layer has its own cache, so each layer's
 working set (about 1.2 GB) is far larger than L2 and no flush is needed.
 
@@ -317,26 +318,20 @@ def run_pkv(args, rank, world, local):
     maxctx = w.max_context_len
     stream = torch.cuda.current_stream(device)
 
-    dec_events = []
-
-    def step(record: bool):
+    def step():
+        # one layer = the KV write fused into decode (rows a1 + a2 in one call);
+        # nothing else runs in the step, so no event sits between the launches
+        # (an event record would break the programmatic-dependent-launch overlap)
         for l in range(LAYERS):
-            pkv.kv_cache_write(ks[l], vs[l], slots, kv[0, l], kv[1, l])
-            if record:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            pkv.paged_attn_decode(qs[l], kv[0, l], kv[1, l], ctx, tab, w.scale, out=outs[l], workspace=ws,
-                                  max_context_len=maxctx)
-            if record:
-                e1.record(stream)
-                dec_events.append((e0, e1))
+            pkv.paged_attn_decode_fused_write(qs[l], ks[l], vs[l], slots, kv[0, l], kv[1, l], ctx, tab, w.scale,
+                                              out=outs[l], workspace=ws, max_context_len=maxctx)
 
     step_bytes = LAYERS * (decode_bytes(w.context_lens, hq, hkv) + write_bytes(w.slot_mapping, hkv))
-    dec_bytes = decode_bytes(w.context_lens, hq, hkv)
+    dec_bytes = decode_bytes(w.context_lens, hq, hkv) + write_bytes(w.slot_mapping, hkv)
 
     with ClockSampler(local) as clocks:
         for _ in range(max(3, args.warmup)):
-            step(False)
+            step()
         torch.cuda.synchronize()
         assert pkv.device_error() == [], "device error during warm-up"
         barrier(world)
@@ -345,14 +340,16 @@ def run_pkv(args, rank, world, local):
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for _ in range(args.steps):
-            step(True)
+            step()
         t_end.record(stream)
         torch.cuda.synchronize()
         clocks.mark_end()
         barrier(world)
     ms = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms, world, device)
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_events)
+    # average duration of one fused call over the timed region: the region
+    # holds only these calls, back to back, so launch gaps count against it
+    dec_ms = ms / LAYERS
     clk = clocks.summary()
 
     # end to end: per-step inputs from pinned host memory, outputs back to host
@@ -361,21 +358,50 @@ def run_pkv(args, rank, world, local):
     h_v = vs.cpu().pin_memory()
     h_meta = [torch.from_numpy(a).pin_memory() for a in (w.slot_mapping, w.context_lens, w.block_tables)]
     h_out = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
-    d_q, d_k, d_v, d_out = (torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0]),
-                            torch.empty_like(outs[0]))
     d_meta = [torch.empty_like(t, device=device) for t in h_meta]
 
+    # double-buffered device copies of one layer's inputs and output: a copy
+    # stream brings layer l+1's q/k/v from pinned host memory and drains layer
+    # l-1's output while the compute stream runs layer l
+    d_in = [(torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0])) for _ in range(2)]
+    d_res = [torch.empty_like(outs[0]) for _ in range(2)]
+    copy = torch.cuda.Stream(device)
+
     def e2e_step():
-        for dst, src in zip(d_meta, h_meta):
-            dst.copy_(src, non_blocking=True)
+        in_ready = [torch.cuda.Event() for _ in range(LAYERS)]
+        in_free = [torch.cuda.Event() for _ in range(LAYERS)]
+        out_ready = [torch.cuda.Event() for _ in range(LAYERS)]
+        out_free = [torch.cuda.Event() for _ in range(LAYERS)]
+        with torch.cuda.stream(copy):
+            copy.wait_stream(stream)
+            for dst, src in zip(d_meta, h_meta):
+                dst.copy_(src, non_blocking=True)
+
+        def load(l):
+            with torch.cuda.stream(copy):
+                if l >= 2:
+                    copy.wait_event(in_free[l - 2])
+                for dst, src in zip(d_in[l % 2], (h_q[l], h_k[l], h_v[l])):
+                    dst.copy_(src, non_blocking=True)
+                in_ready[l].record(copy)
+
+        load(0)
         for l in range(LAYERS):
-            d_q.copy_(h_q[l], non_blocking=True)
-            d_k.copy_(h_k[l], non_blocking=True)
-            d_v.copy_(h_v[l], non_blocking=True)
-            pkv.kv_cache_write(d_k, d_v, d_meta[0], kv[0, l], kv[1, l])
-            pkv.paged_attn_decode(d_q, kv[0, l], kv[1, l], d_meta[1], d_meta[2], w.scale, out=d_out, workspace=ws,
-                                  max_context_len=maxctx)
-            h_out[l].copy_(d_out, non_blocking=True)
+            if l + 1 < LAYERS:
+                load(l + 1)
+            stream.wait_event(in_ready[l])
+            if l >= 2:
+                stream.wait_event(out_free[l - 2])
+            dq, dk, dv = d_in[l % 2]
+            pkv.paged_attn_decode_fused_write(dq, dk, dv, d_meta[0], kv[0, l], kv[1, l], d_meta[1], d_meta[2],
+                                              w.scale, out=d_res[l % 2], workspace=ws, max_context_len=maxctx)
+            in_free[l].record(stream)
+            out_ready[l].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(out_ready[l])
+                h_out[l].copy_(d_res[l % 2], non_blocking=True)
+                out_free[l].record(copy)
+        stream.wait_stream(copy)
 
     for _ in range(2):
         e2e_step()
@@ -397,11 +423,6 @@ def run_pkv(args, rank, world, local):
     # as a CUDA graph (bucket = batch) and replayed
     from paged_kv_cache_304_gb300.graphs import DecodeGraphRunner
 
-    def fused_step():
-        for l in range(LAYERS):
-            pkv.paged_attn_decode_fused_write(qs[l], ks[l], vs[l], slots, kv[0, l], kv[1, l], ctx, tab, w.scale,
-                                              out=outs[l], workspace=ws, max_context_len=maxctx)
-
     def timed(fn):
         for _ in range(3):
             fn()
@@ -422,9 +443,16 @@ def run_pkv(args, rank, world, local):
         gms = timed(runner.graphs[B].replay)
         extra[name] = {"ms_per_step": round(gms, 4), "GB/s": round(step_bytes * world / (gms / 1e3) / 1e9, 2)}
         del runner
-    fms = timed(fused_step)
-    extra["decode_step_fused_write"] = {"ms_per_step": round(fms, 4),
-                                        "GB/s": round(step_bytes * world / (fms / 1e3) / 1e9, 2)}
+    def unfused_step():
+        for l in range(LAYERS):
+            pkv.kv_cache_write(ks[l], vs[l], slots, kv[0, l], kv[1, l])
+            pkv.paged_attn_decode(qs[l], kv[0, l], kv[1, l], ctx, tab, w.scale, out=outs[l], workspace=ws,
+                                  max_context_len=maxctx)
+
+    ums = timed(unfused_step)
+    extra["decode_step_separate_write"] = {"ms_per_step": round(ums, 4),
+                                           "GB/s": round(step_bytes * world / (ums / 1e3) / 1e9, 2),
+                                           "note": "kv_cache_write then paged_attn_decode per layer (eager)"}
     if not args.no_extra:
         extra.update(run_extras(torch, pkv, device, gen, pk))
     assert pkv.device_error() == [], "device error during the benchmark"
@@ -444,7 +472,7 @@ def run_pkv(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "qwen3_0.6b_decode_b256: 28 layers x (kv_cache_write + paged_attn_decode)",
+        "config": {"workload": "qwen3_0.6b_decode_b256: 28 layers x paged_attn_decode_fused_write (KV write + decode)",
                    "batch": B, "context_lens": "U[100, 2048], seed 3042", "layers": LAYERS, "num_q_heads": hq,
                    "num_kv_heads": hkv, "head_dim": d, "block_size": 256, "num_blocks_per_layer": w.num_blocks,
                    "l2": "inputs larger than L2 (about 1.2 GB per layer, a different cache per layer)",
@@ -452,13 +480,14 @@ def run_pkv(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(dec_gbs / NOMINAL_HBM_GBS, 4),
-                     "kernel": "paged_attn_decode (decode_kernel + decode_combine_kernel)",
+                     "kernel": "paged_attn_decode_fused_write call (decode_kernel with the KV write, then "
+                               "decode_combine_kernel); time per call = timed region / calls",
                      "bytes_per_launch": dec_bytes, "ms_per_launch": round(dec_ms, 5),
                      "traffic": recorded_traffic() if LAYERS == 28 or LAYERS == 1 else None},
         "clocks": clk,
         "e2e": {"value": round(step_bytes * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * LAYERS * 3,
+        "gpu_launches": args.steps * LAYERS * 2,
         "extra": extra,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
