@@ -15,20 +15,26 @@
 // pipe always has one slot's work while the other slot's softmax runs.
 // * warp 0, producer: TMA-loads the two Q tiles, then streams the kv head's
 //   128-token K and V tiles (two per 256-token cache block, looked up in the
-//   block table) into 2-stage rings, as 64-dim halves of 128 rows x 128 bytes
-//   with the 128-byte swizzle.
-// * warp 1, MMA: one thread issues tcgen05.mma (kind::f16, bf16 in, fp32
-//   accumulate).  Tensor memory holds S_A | S_B | O_A | O_B (128 columns
-//   each).  Order per K/V tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1); the
-//   probabilities P_X(j) are written over S_X(j) as packed bf16 and read as
-//   the A operand straight from tensor memory.
+//   block table) into rings of three K and two V stages, as 64-dim halves
+//   of 128 rows x 128 bytes with the 128-byte swizzle.
+// * warps 1 (slot A) and 10 (slot B), MMA: one thread per slot issues
+//   tcgen05.mma (kind::f16, bf16 in, fp32 accumulate); an issuing thread
+//   stays blocked while its instructions queue behind the tensor pipe, so
+//   one issuer per slot lets one slot's waits overlap the other's MMAs.
+//   Tensor memory holds S (128 columns, shared by the slots), P_A | P_B (64
+//   columns each, packed bf16) and O_A | O_B (128 each).  The S columns are
+//   handed from slot to slot, S_A(0), S_B(0), S_A(1), ..., each S issued as
+//   soon as the previous one has been read into registers, so the next
+//   tile's S never waits for this tile's P V.  Matrix descriptors are built
+//   once; a k-step adds a constant.
 // * warps 2-5 (slot A) and 6-9 (slot B), softmax: warp w reads TMEM lanes
-//   32 (w % 4) .. +31, so thread r of a group owns query row r (TMEM lane r).  It loads its 128 scores with tcgen05.ld, applies the
-//   causal mask on diagonal tiles, keeps the running row maximum (log2
-//   units, scale * log2(e) folded in; reductions split over 8 independent
-//   accumulators), rescales O in tensor memory only when the maximum grew by
-//   more than 2^8, and stores P.  At the end it normalises O by the row sum
-//   and writes bf16 rows.
+//   32 (w % 4) .. +31, so thread r of a group owns query row r (TMEM lane
+//   r).  It loads its 128 scores with tcgen05.ld, releases the S columns,
+//   applies the causal mask on diagonal tiles, keeps the running row maximum
+//   (log2 units, scale * log2(e) folded in), waits for the previous P V of
+//   its slot, rescales O in tensor memory only when the maximum grew by
+//   more than 2^8, and stores P.  At the end it normalises O by the row sum,
+//   stages the bf16 rows in shared memory and writes whole rows.
 // * Tiles are launched heaviest first (the last query tile of a sequence
 //   sees the most keys); the hardware block scheduler balances the rest.
 // Every wait is bounded (two seconds); on timeout the CTA flags
@@ -45,8 +51,9 @@ __device__ unsigned int g_err_prefill;
 
 constexpr int kTileM = 128;    // query rows per slot
 constexpr int kTileN = 128;    // keys per K/V tile
-constexpr int kKvStages = 2;
-constexpr int kThreads = 320;  // 10 warps: producer, MMA, 4 softmax A, 4 softmax B
+constexpr int kKStages = 3;  // K tiles in flight: K(j+3) loads once S(j) of both slots is done
+constexpr int kVStages = 2;  // V tiles in flight
+constexpr int kThreads = 352;  // 11 warps: producer, MMA A, 4 softmax A, 4 softmax B, MMA B
 constexpr uint32_t kTileBytes = kTileN * kHeadDim * 2;  // 32 KiB: one Q, K or V tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;         // one 64-dim half
 constexpr uint32_t kTmemCols = 512;
@@ -65,15 +72,17 @@ struct PrefillParams {
 // Shared memory: Q_A | Q_B | K stages | V stages | barriers.
 struct Smem {
   uint8_t* q;   // 2 tiles
-  uint8_t* k0;  // kKvStages tiles
-  uint8_t* v0;  // kKvStages tiles
+  uint8_t* k0;  // kKStages tiles
+  uint8_t* v0;  // kVStages tiles
   uint64_t* q_full;
-  uint64_t* k_full;   // [kKvStages]
-  uint64_t* k_empty;  // [kKvStages]
-  uint64_t* v_full;   // [kKvStages]
-  uint64_t* v_empty;  // [kKvStages]
-  uint64_t* s_full;   // [2 slots]
-  uint64_t* p_full;   // [2 slots]
+  uint64_t* k_full;   // [kKStages]
+  uint64_t* k_empty;  // [kKStages]
+  uint64_t* v_full;   // [kVStages]
+  uint64_t* v_empty;  // [kVStages]
+  uint64_t* s_full;   // [2 slots]: S of this slot computed
+  uint64_t* s_free;   // [2 slots]: the shared S columns may take this slot's next S
+  uint64_t* p_full;   // [2 slots]: P of this slot stored
+  uint64_t* pv_done;  // [2 slots]: P V of this slot completed (P columns and O reusable)
   uint64_t* o_done;   // [2 slots]
   uint32_t* tmem_base;
 };
@@ -82,21 +91,24 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   Smem s;
   s.q = base;
   s.k0 = base + 2 * kTileBytes;
-  s.v0 = s.k0 + kKvStages * kTileBytes;
-  uint64_t* b = reinterpret_cast<uint64_t*>(s.v0 + kKvStages * kTileBytes);
+  s.v0 = s.k0 + kKStages * kTileBytes;
+  uint64_t* b = reinterpret_cast<uint64_t*>(s.v0 + kVStages * kTileBytes);
   s.q_full = b;
   s.k_full = b + 1;
-  s.k_empty = s.k_full + kKvStages;
-  s.v_full = s.k_empty + kKvStages;
-  s.v_empty = s.v_full + kKvStages;
-  s.s_full = s.v_empty + kKvStages;
-  s.p_full = s.s_full + 2;
-  s.o_done = s.p_full + 2;
+  s.k_empty = s.k_full + kKStages;
+  s.v_full = s.k_empty + kKStages;
+  s.v_empty = s.v_full + kVStages;
+  s.s_full = s.v_empty + kVStages;
+  s.s_free = s.s_full + 2;
+  s.p_full = s.s_free + 2;
+  s.pv_done = s.p_full + 2;
+  s.o_done = s.pv_done + 2;
   s.tmem_base = reinterpret_cast<uint32_t*>(s.o_done + 2);
   return s;
 }
 
-constexpr size_t kSmemBytes = 1024 + (2 + 2 * kKvStages) * kTileBytes + 32 * sizeof(uint64_t) + 16;
+constexpr size_t kSmemBytes = 1024 + (2 + kKStages + kVStages) * kTileBytes + 32 * sizeof(uint64_t) + 16;
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 __device__ __forceinline__ int load_block(const PrefillParams& p, int seq, int lb) {
   int phys = __ldg(p.tables + static_cast<int64_t>(seq) * p.maxb + lb);
@@ -120,25 +132,30 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const CUten
   }
 }
 
+// Matrix descriptors are built once per CTA; a k-step only adds a constant to
+// the 16-byte address field in the low bits (the addresses stay below
+// 256 KiB, so the add never carries out of the field).  Rebuilding the 64-bit
+// descriptor for every instruction made the single issuing thread, not the
+// tensor pipe, the limit.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // S = Q K^T: A = Q tile, B = K tile, both K-major (dims contiguous) with the
 // 128-byte swizzle; k-step kk selects 32 bytes of a 64-dim half.
-__device__ __forceinline__ void issue_s(uint32_t d, uint32_t qa, uint32_t ka) {
+__device__ __forceinline__ void issue_s(uint32_t d, uint64_t qdesc, uint64_t kdesc) {
 #pragma unroll
   for (int kk = 0; kk < kHeadDim / 16; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    tc::mma_ss(d, tc::smem_desc_sw128(qa + off, 16, 1024), tc::smem_desc_sw128(ka + off, 16, 1024), kIdescS,
-               kk > 0);
+    tc::mma_ss(d, desc_add(qdesc, off), desc_add(kdesc, off), kIdescS, kk > 0);
   }
 }
 
 // O += P V with P (128 x 128 keys, packed bf16) in tensor memory at `p_tmem`
 // and V (keys x dims, dims contiguous) in shared memory: 64-dim halves are
 // 16 KiB apart (leading offset), 8-key groups 1 KiB apart (stride offset).
-__device__ __forceinline__ void issue_pv(uint32_t o, uint32_t p_tmem, uint32_t va, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t o, uint32_t p_tmem, uint64_t vdesc, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < kTileN / 16; ++kk)
-    tc::mma_ts(o, p_tmem + kk * 8, tc::smem_desc_sw128(va + kk * 2048, kHalfBytes, 1024), kIdescPV,
-               (acc || kk > 0) ? 1u : 0u);
+    tc::mma_ts(o, p_tmem + kk * 8, desc_add(vdesc, kk * 2048), kIdescPV, (acc || kk > 0) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -175,19 +192,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem sm = carve(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // The producer's first block-table entries and the tensor-map prefetches
+  // are issued before the barrier set-up so their latency overlaps it.
+  int phys = 0, nxt = 0;
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    phys = load_block(p, seq, 0);
+    nxt = nkv > 2 ? load_block(p, seq, 1) : 0;
+  }
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full, 1);
-    for (int i = 0; i < kKvStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&sm.k_full[i], 1);
-      mbar_init(&sm.k_empty[i], 1);
+      mbar_init(&sm.k_empty[i], has_b ? 2 : 1);  // released by each slot's S
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.v_empty[i], 1);
+      mbar_init(&sm.v_empty[i], has_b ? 2 : 1);  // released by each slot's P V
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.pv_done[i], 1);
       mbar_init(&sm.o_done[i], 1);
     }
+    mbar_init(&sm.s_free[0], 4);
+    mbar_init(&sm.s_free[1], 4);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -198,14 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *sm.tmem_base;
-  // columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511
+  // columns: S 0-127, P_A 128-191, P_B 192-255, O_A 256-383, O_B 384-511
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensormap(&qmap);
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
       const int row0 = q0 + kTileM * m;
       mbar_arrive_expect_tx(sm.q_full, has_b ? 2 * kTileBytes : kTileBytes);
       tma_load_3d(sm.q, &qmap, sm.q_full, 0, hA, row0);
@@ -214,79 +243,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sm.q + kTileBytes, &qmap, sm.q_full, 0, hA + 1, row0);
         tma_load_3d(sm.q + kTileBytes + kHalfBytes, &qmap, sm.q_full, 64, hA + 1, row0);
       }
-      int phys = load_block(p, seq, 0);
-      int nxt = nkv > 2 ? load_block(p, seq, 1) : 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % kKvStages;
-        const uint32_t par = ((j / kKvStages) & 1) ^ 1;
-        if ((j & 1) == 0 && j > 0) {
-          phys = nxt;
-          if (2 * (j / 2 + 1) < nkv) nxt = load_block(p, seq, j / 2 + 1);
+      // Order K(0), K(1), V(0), K(2), V(1), ...: the MMA warp needs K(j+1)
+      // (for the next S) before V(j) (for this tile's P V).
+      int phys_v = phys;  // block of the next V tile
+      for (int j = 0; j <= nkv; ++j) {
+        if (j < nkv) {
+          if ((j & 1) == 0 && j > 0) {
+            phys = nxt;
+            if (2 * (j / 2 + 1) < nkv) nxt = load_block(p, seq, j / 2 + 1);
+          }
+          const int sk = j % kKStages;
+          if (!mbar_wait(&sm.k_empty[sk], ((j / kKStages) & 1) ^ 1, &g_err_prefill)) break;
+          mbar_arrive_expect_tx(&sm.k_full[sk], kTileBytes);
+          load_kv_tile(p, &kmap, sm.k0 + sk * kTileBytes, &sm.k_full[sk], phys, (j & 1) * kTileN, g);
         }
-        const int tin = (j & 1) * kTileN;
-        if (!mbar_wait(&sm.k_empty[st], par, &g_err_prefill)) break;
-        mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-        load_kv_tile(p, &kmap, sm.k0 + st * kTileBytes, &sm.k_full[st], phys, tin, g);
-        if (!mbar_wait(&sm.v_empty[st], par, &g_err_prefill)) break;
-        mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-        load_kv_tile(p, &vmap, sm.v0 + st * kTileBytes, &sm.v_full[st], phys, tin, g);
+        if (j > 0) {
+          const int jv = j - 1, sv = jv % kVStages;
+          if (!mbar_wait(&sm.v_empty[sv], ((jv / kVStages) & 1) ^ 1, &g_err_prefill)) break;
+          mbar_arrive_expect_tx(&sm.v_full[sv], kTileBytes);
+          load_kv_tile(p, &vmap, sm.v0 + sv * kTileBytes, &sm.v_full[sv], phys_v, (jv & 1) * kTileN, g);
+          if (jv & 1) phys_v = phys;  // V(jv + 1) starts the block K(j) is in
+        }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (warp == 10 && has_b)) {
     // ------------------------------------------------------------ MMA issue
+    // One issuing thread per slot (warp 1: A, warp 10: B).  An issuing thread
+    // stays blocked while its MMAs queue behind the tensor pipe, so with one
+    // thread per slot one slot's waits overlap the other slot's MMAs.
     if (lane == 0) {
-      const uint32_t qa = smem_u32(sm.q), qb = qa + kTileBytes;
-      const uint32_t sA = tmem, sB = tmem + 128, oA = tmem + 256, oB = tmem + 384;
+      const int slot = warp == 1 ? 0 : 1;
+      const uint32_t qa = smem_u32(sm.q), k0a = smem_u32(sm.k0), v0a = smem_u32(sm.v0);
+      const uint64_t qd = desc_add(tc::smem_desc_sw128(qa, 16, 1024), slot * kTileBytes);
+      const uint64_t kd0 = tc::smem_desc_sw128(k0a, 16, 1024);
+      const uint64_t vd0 = tc::smem_desc_sw128(v0a, kHalfBytes, 1024);
+      const uint32_t sT = tmem, pX = tmem + 128 + 64 * slot, oX = tmem + 256 + 128 * slot;
+      // The S columns are handed over S_A(0), S_B(0), S_A(1), ...: S_X(j)
+      // waits for s_free[X] phase j - 1 (slot A) or j (slot B), completed
+      // when the other slot (or, with one slot, this one) has read its S.
       bool ok = mbar_wait(sm.q_full, 0, &g_err_prefill) && mbar_wait(&sm.k_full[0], 0, &g_err_prefill);
+      if (ok && slot == 1) ok = mbar_wait(&sm.s_free[1], 0, &g_err_prefill);
       if (ok) {
         tc::fence_after();
-        const uint32_t ka = smem_u32(sm.k0);
-        issue_s(sA, qa, ka);
-        tc::commit(&sm.s_full[0]);
-        if (has_b) {
-          issue_s(sB, qb, ka);
-          tc::commit(&sm.s_full[1]);
-        }
+        issue_s(sT, qd, kd0);
+        tc::commit(&sm.s_full[slot]);
         tc::commit(&sm.k_empty[0]);
       }
       for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j % kKvStages;
+        const int sv = j % kVStages;
         const bool more = j + 1 < nkv;
-        const int st1 = (j + 1) % kKvStages;
-        if (!mbar_wait(&sm.v_full[st], (j / kKvStages) & 1, &g_err_prefill)) break;
-        if (!mbar_wait(&sm.p_full[0], j & 1, &g_err_prefill)) break;
-        tc::fence_after();
-        const uint32_t va = smem_u32(sm.v0 + st * kTileBytes);
-        issue_pv(oA, sA, va, j > 0);
-        if (!more) tc::commit(&sm.o_done[0]);
+        const int st1 = (j + 1) % kKStages;
         if (more) {
-          if (!mbar_wait(&sm.k_full[st1], ((j + 1) / kKvStages) & 1, &g_err_prefill)) break;
+          if (!mbar_wait(&sm.s_free[slot], (slot == 0 ? j : j + 1) & 1, &g_err_prefill)) break;
+          if (!mbar_wait(&sm.k_full[st1], ((j + 1) / kKStages) & 1, &g_err_prefill)) break;
           tc::fence_after();
-          issue_s(sA, qa, smem_u32(sm.k0 + st1 * kTileBytes));
-          tc::commit(&sm.s_full[0]);
+          issue_s(sT, qd, desc_add(kd0, st1 * kTileBytes));
+          tc::commit(&sm.s_full[slot]);
+          tc::commit(&sm.k_empty[st1]);
         }
-        if (has_b) {
-          if (!mbar_wait(&sm.p_full[1], j & 1, &g_err_prefill)) break;
-          tc::fence_after();
-          issue_pv(oB, sB, va, j > 0);
-          if (!more) tc::commit(&sm.o_done[1]);
-          if (more) {
-            issue_s(sB, qb, smem_u32(sm.k0 + st1 * kTileBytes));
-            tc::commit(&sm.s_full[1]);
-          }
-        }
-        tc::commit(&sm.v_empty[st]);
-        if (more) tc::commit(&sm.k_empty[st1]);
+        if (!mbar_wait(&sm.p_full[slot], j & 1, &g_err_prefill)) break;
+        if (!mbar_wait(&sm.v_full[sv], (j / kVStages) & 1, &g_err_prefill)) break;
+        tc::fence_after();
+        issue_pv(oX, pX, desc_add(vd0, sv * kTileBytes), j > 0);
+        tc::commit(&sm.pv_done[slot]);
+        if (!more) tc::commit(&sm.o_done[slot]);
+        tc::commit(&sm.v_empty[sv]);
       }
     }
-  } else if (warp >= 2 && (warp < 6 || has_b)) {
+  } else if (warp >= 2 && warp < 10 && (warp < 6 || has_b)) {
     // ------------------------------------------------------------ softmax + epilogue
     const int slot = warp >= 6 ? 1 : 0;
     const int h = hA + slot;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_addr = tmem + slot * 128 + lane_bits;
+    const uint32_t s_addr = tmem + lane_bits;                   // shared S columns
+    const uint32_t p_addr = tmem + 128 + slot * 64 + lane_bits;  // this slot's P
     const uint32_t o_addr = tmem + 256 + slot * 128 + lane_bits;
     const int lim_row = c + kTileM * m + r;  // last visible key of this row
     float m_ref = -INFINITY, l = 0.f;
@@ -309,6 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::ld32(s_addr + 64, s + 64);
       tc::ld32(s_addr + 96, s + 96);
       tc::wait_ld();
+      // S is in registers: let the MMA warp reuse the S columns.
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[(slot == 0 && has_b) ? 1 : 0]);
       if (wdiag) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -332,9 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
       }
       const float mu = m_ref;  // finite: key 0 is visible to every row
-      // p = 2^(s * scale * log2e - m), packed to bf16 pairs and written over
-      // S 32 keys at a time: keys 32q..32q+31 go to columns 16q..16q+15, which
-      // hold scores already in registers.
+      // P_X(j-1) must be consumed (and O_X stable) before P_X(j) is stored.
+      if (j > 0) {
+        if (!mbar_wait(&sm.pv_done[slot], (j - 1) & 1, &g_err_prefill)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+      }
+      // p = 2^(s * scale * log2e - m), packed to bf16 pairs and stored in
+      // this slot's P columns 32 keys at a time (keys 32q..32q+31 go to
+      // columns 16q..16q+15).
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const float2 sl2 = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
 #pragma unroll
@@ -347,9 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           rs[(x >> 1) & 3] = fadd2(rs[(x >> 1) & 3], e);
           pk[x >> 1] = pack_bf16x2(e.x, e.y);
         }
-        tc::st16u(s_addr + 16 * q, pk);
+        tc::st16u(p_addr + 16 * q, pk);
       }
-      // O_X is stable here: S_X(j) completing implies PV_X(j-1) completed.
+      // O_X is stable here: PV_X(j-1) has completed (pv_done above).
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -372,24 +416,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && mbar_wait(&sm.o_done[slot], 0, &g_err_prefill)) {
       tc::fence_after();
       const float inv = fast_rcp(l);
-      const int row = kTileM * m + r;
-      uint16_t* dst = p.out + (static_cast<int64_t>(q0 + row) * p.Hq + h) * kHeadDim;
+      // Stage the bf16 row in this slot's Q buffer (free: o_done implies
+      // every MMA of the CTA that reads Q has completed): 16-byte chunk c of
+      // row r goes to chunk c ^ (r % 16), so the 32 rows of a warp hit all
+      // banks.  Then the warp writes its 32 rows out two full rows per
+      // instruction instead of 32 scattered 16-byte pieces.
+      fence_proxy_async_smem();
+      uint8_t* stage = sm.q + slot * kTileBytes;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float o[32];
-        tc::ld32(o_addr + cc * 32, o);
+      for (int hh = 0; hh < 2; ++hh) {
+        float o[64];
+        tc::ld32(o_addr + 64 * hh, o);
+        tc::ld32(o_addr + 64 * hh + 32, o + 32);
         tc::wait_ld();
-        if (row < n) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 8) {
-            const uint32_t w0 = pack_bf16x2(o[x] * inv, o[x + 1] * inv);
-            const uint32_t w1 = pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv);
-            const uint32_t w2 = pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv);
-            const uint32_t w3 = pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv);
-            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + cc * 32 + x), "r"(w0), "r"(w1),
-                         "r"(w2), "r"(w3)
-                         : "memory");
-          }
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const float* v = o + 8 * c8;
+          const int c16 = 8 * hh + c8;
+          uint4 w;
+          w.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+          w.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+          w.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+          w.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+          *reinterpret_cast<uint4*>(stage + r * 256 + ((c16 ^ (r & 15)) << 4)) = w;
+        }
+      }
+      __syncwarp();
+      const int ch = lane & 15;
+      const int64_t row_stride = static_cast<int64_t>(p.Hq) * kHeadDim;  // elements between token rows
+      uint16_t* dst0 = p.out + static_cast<int64_t>(q0 + kTileM * m) * row_stride + h * kHeadDim + ch * 8;
+      const int rows_left = n - kTileM * m;  // rows of this tile inside the sequence
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int tr = 32 * wq + 2 * i + (lane >> 4);  // tile row written by this lane
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + tr * 256 + ((ch ^ (tr & 15)) << 4));
+        if (tr < rows_left) {
+          uint16_t* dst = dst0 + tr * row_stride;
+          asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
+                       "r"(w.w)
+                       : "memory");
         }
       }
     }
