@@ -148,22 +148,38 @@ __device__ __forceinline__ int load_block(const DecodeParams& p, int b, int lb) 
 // a padding row (nothing written); any other value is flagged and skipped,
 // since writing elsewhere could race with other CTAs' reads.
 __device__ void write_new_token(const DecodeParams& p, int b, int L, int lane) {
-  const int s = __ldg(p.slots + b);
-  if (s == -1) return;
+  // The slot, its table entry and the new rows are loaded together (one
+  // round of latency on the producer's path), then checked and stored.
+  constexpr int kVecsPerLane = kMaxKvHeads * kHeadDim / 8 / 32;  // 16-byte chunks of a row per lane
   const int pos = L - 1;
+  const int row_vecs = p.Hkv * kHeadDim / 8;
+  const int s = __ldg(p.slots + b);
   const int phys = __ldg(p.tables + static_cast<int64_t>(b) * p.maxb + pos / kBlockSize);
+  const uint4* ks = p.k_new + static_cast<int64_t>(b) * p.k_stride_vec;
+  const uint4* vs = p.v_new + static_cast<int64_t>(b) * p.v_stride_vec;
+  uint4 kr[kVecsPerLane], vr[kVecsPerLane];
+#pragma unroll
+  for (int i = 0; i < kVecsPerLane; ++i) {
+    const int c = lane + 32 * i;
+    if (c < row_vecs) {
+      kr[i] = __ldg(ks + c);
+      vr[i] = __ldg(vs + c);
+    }
+  }
+  if (s == -1) return;
   if (phys < 0 || phys >= p.num_blocks || s != phys * kBlockSize + pos % kBlockSize) {
     if (lane == 0) atomicOr(&g_err_decode, PKV_DEVERR_SLOT_RANGE);
     return;
   }
-  const int row_vecs = p.Hkv * kHeadDim / 8;
-  const uint4* ks = p.k_new + static_cast<int64_t>(b) * p.k_stride_vec;
-  const uint4* vs = p.v_new + static_cast<int64_t>(b) * p.v_stride_vec;
   uint4* kd = p.k_cache_w + static_cast<int64_t>(s) * row_vecs;
   uint4* vd = p.v_cache_w + static_cast<int64_t>(s) * row_vecs;
-  for (int c = lane; c < row_vecs; c += 32) {
-    kd[c] = __ldg(ks + c);
-    vd[c] = __ldg(vs + c);
+#pragma unroll
+  for (int i = 0; i < kVecsPerLane; ++i) {
+    const int c = lane + 32 * i;
+    if (c < row_vecs) {
+      kd[c] = kr[i];
+      vd[c] = vr[i];
+    }
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -171,10 +187,10 @@ __device__ void write_new_token(const DecodeParams& p, int b, int L, int lane) {
 // Issue every tile of unit (b, [lo, hi)).  Lane 0 of the producer warp only.
 __device__ void emit_unit(const DecodeParams& p, const Smem& sm, const CUtensorMap* kmap,
                           const CUtensorMap* vmap, ProducerState& ps, int b, int lo, int hi, int L,
-                          int slot) {
+                          int slot, int first_phys) {
   const int t_begin = lo & ~(kT - 1);
   int lb_cur = -1, phys = 0;
-  int nxt = load_block(p, b, t_begin >> 8);
+  int nxt = first_phys;  // block of token t_begin, looked up ahead by the warp
   for (int t = t_begin; t < hi && ps.ok; t += kT) {
     const int lb = t >> 8;
     if (lb != lb_cur) {
@@ -268,6 +284,8 @@ __device__ void producer(const DecodeParams& p, const Smem& sm, const CUtensorMa
       unsigned mask = __ballot_sync(0xffffffffu, has);
       const int lo_rel = has ? static_cast<int>(lo - Sb) : 0;
       const int hi_rel = has ? static_cast<int>(hi - Sb) : 0;
+      // the first block of every piece of this batch, looked up together
+      const int first_phys = has ? load_block(p, b, lo_rel >> 8) : 0;
       while (mask) {
         const int j = __ffs(mask) - 1;
         mask &= mask - 1;
@@ -275,9 +293,10 @@ __device__ void producer(const DecodeParams& p, const Smem& sm, const CUtensorMa
         const int loj = __shfl_sync(0xffffffffu, lo_rel, j);
         const int hij = __shfl_sync(0xffffffffu, hi_rel, j);
         const int Lj = __shfl_sync(0xffffffffu, L, j);
+        const int physj = __shfl_sync(0xffffffffu, first_phys, j);
         if (p.fuse_write && hij == Lj) write_new_token(p, bj, Lj, lane);
         __syncwarp();
-        if (lane == 0 && ps.ok) emit_unit(p, sm, kmap, vmap, ps, bj, loj, hij, Lj, bj + blockIdx.x);
+        if (lane == 0 && ps.ok) emit_unit(p, sm, kmap, vmap, ps, bj, loj, hij, Lj, bj + blockIdx.x, physj);
         ps.ok = __shfl_sync(0xffffffffu, ps.ok, 0);
         ps.it = __shfl_sync(0xffffffffu, ps.it, 0);
         ps.units = __shfl_sync(0xffffffffu, ps.units, 0);
