@@ -239,6 +239,16 @@ def oracle_decode_layer_rate(min_seconds: float = 10.0, max_reps: int = 20):
     return gbs, oracle.num_threads(), desc
 
 
+def step_config(w, world: int) -> dict:
+    """The `config` of the benchmark step (the same for both arms)."""
+    return {"workload": "qwen3_0.6b_decode_b256: 28 layers x paged_attn_decode_fused_write (KV write + decode)",
+            "batch": w.batch, "context_lens": "U[100, 2048], seed 3042", "layers": LAYERS,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 128, "block_size": 256,
+            "num_blocks_per_layer": w.num_blocks,
+            "l2": "inputs larger than L2 (about 1.2 GB per layer, a different cache per layer)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     """The reference arm: the fp64 CPU oracle, timed on the host cores."""
     if rank != 0:
@@ -266,11 +276,10 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "qwen3_0.6b_decode_b256 (sample: 32 of 256 sequences, 1 of 28 layers)",
-                   "batch": 256, "layers": LAYERS, "num_q_heads": 16, "num_kv_heads": 8, "head_dim": 128,
-                   "block_size": 256},
+        "config": step_config(w, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": "32 of 256 sequences of one layer, KV write + decode per step"},
+                         "sample": "each step: the KV write and decode of 32 of the 256 sequences of one of the "
+                                   "28 layers, GB/s of those algorithmic bytes"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -467,11 +476,7 @@ def run_pkv(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "qwen3_0.6b_decode_b256: 28 layers x paged_attn_decode_fused_write (KV write + decode)",
-                   "batch": B, "context_lens": "U[100, 2048], seed 3042", "layers": LAYERS, "num_q_heads": hq,
-                   "num_kv_heads": hkv, "head_dim": d, "block_size": 256, "num_blocks_per_layer": w.num_blocks,
-                   "l2": "inputs larger than L2 (about 1.2 GB per layer, a different cache per layer)",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(w, world),
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(dec_gbs / NOMINAL_HBM_GBS, 4),
