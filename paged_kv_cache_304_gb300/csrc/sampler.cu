@@ -16,7 +16,7 @@
 // i % 4 of Philox(counter = {i / 4, b, offset_lo, offset_hi},
 // key = {seed_lo, seed_hi}); U = ((word >> 9) + 0.5) / 2^23 in (0, 1).
 //
-// Kernels: a grid of (4096-token chunk, row) CTAs streams the logits with
+// Kernels: a grid of (8192-token chunk, row) CTAs streams the logits with
 // 16-byte loads, generates the noise in registers and reduces (key, index) to
 // one partial per chunk (ties go to the smaller index); a second kernel (one
 // warp per row) reduces the partials.  The pass is bound by HBM: 4 bytes of
@@ -31,8 +31,8 @@ namespace {
 
 __device__ unsigned int g_err_sampler;
 
-constexpr int kChunk = 4096;
-constexpr int kThreads = 256;  // 16 tokens per thread
+constexpr int kChunk = 8192;
+constexpr int kThreads = 256;  // 32 tokens per thread
 
 struct SampleParams {
   const float* logits;

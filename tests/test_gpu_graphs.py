@@ -62,6 +62,31 @@ def test_graph_replay_equals_direct_calls(setup, B):
     assert pkv.device_error() == []
 
 
+@pytest.mark.parametrize("B", [5, 256])
+def test_fused_graph_replay_equals_direct_fused_calls(setup, B):
+    """The runner capturing paged_attn_decode_fused_write (write inside the
+    decode kernel) replays to the direct fused calls, bit for bit."""
+    w, layers_host, qs, ks, vs = setup
+    g_layers = _dev_layers(layers_host)
+    d_layers = _dev_layers(layers_host)
+    runner = DecodeGraphRunner(g_layers, 16, w.max_blocks_per_seq, w.scale, max_batch=512,
+                               max_context_len=w.max_context_len, fused=True)
+    q = torch.stack([to_dev(x[:B]) for x in qs])
+    k = torch.stack([to_dev(x[:B]) for x in ks])
+    v = torch.stack([to_dev(x[:B]) for x in vs])
+    slots, ctx, tab = i32(w.slot_mapping[:B]), i32(w.context_lens[:B]), i32(w.block_tables[:B])
+    out_g = runner.run(q, k, v, slots, ctx, tab).clone()
+    outs_d = [pkv.paged_attn_decode_fused_write(q[li], k[li], v[li], slots, kc, vc, ctx, tab, w.scale,
+                                                max_context_len=w.max_context_len)
+              for li, (kc, vc) in enumerate(d_layers)]
+    torch.cuda.synchronize()
+    for li in range(2):
+        assert torch.equal(out_g[li], outs_d[li]), f"layer {li}"
+        assert torch.equal(g_layers[li][0], d_layers[li][0]) and torch.equal(g_layers[li][1], d_layers[li][1])
+    assert bool((runner.static.out[:, B:runner.bucket(B)] == 0).all()), "pad rows must be zero"
+    assert pkv.device_error() == []
+
+
 def test_graph_replays_repeat_and_match_oracle(setup):
     w, layers_host, qs, ks, vs = setup
     B = 77
