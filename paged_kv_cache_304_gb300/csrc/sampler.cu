@@ -17,10 +17,12 @@
 // key = {seed_lo, seed_hi}); U = ((word >> 9) + 0.5) / 2^23 in (0, 1).
 //
 // Kernels: a grid of (8192-token chunk, row) CTAs streams the logits with
-// 16-byte loads, generates the noise in registers and reduces (key, index) to
-// one partial per chunk (ties go to the smaller index); a second kernel (one
-// warp per row) reduces the partials.  The pass is bound by HBM: 4 bytes of
-// logits per token.
+// 16-byte loads (all of a thread's loads issued first), generates the noise
+// in registers and reduces (key, index) to one partial per chunk (ties go to
+// the smaller index); a second kernel (one warp per row) reduces the
+// partials.  The pass moves 4 bytes of logits per token; at a Qwen3-sized
+// vocabulary it is bound by instruction issue (a quarter Philox block and
+// two logarithms per token) rather than by HBM.
 #include <cuda_runtime.h>
 
 #include "pkv_device.cuh"
@@ -90,7 +92,8 @@ __device__ __forceinline__ void better(float& bk, int& bi, float k, int i) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) sample_chunk_kernel(const SampleParams p) {
+// 64 registers per thread (4 CTAs per SM) hold the eight logit quads in flight.
+__global__ void __launch_bounds__(kThreads, 4) sample_chunk_kernel(const SampleParams p) {
   griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x / p.nchunks;
@@ -102,6 +105,17 @@ __global__ void __launch_bounds__(kThreads) sample_chunk_kernel(const SamplePara
     const float scale = 1.4426950408889634f / T;
     const float* row = p.logits + static_cast<int64_t>(b) * p.row_stride;
     const int base = chunk * kChunk;
+    // All of this thread's logits are requested before any noise is drawn,
+    // so the loads overlap each other and the Philox arithmetic.
+    constexpr int kQuads = kChunk / (4 * kThreads);
+    float4 lv[kQuads];
+    if (p.vec4) {
+#pragma unroll
+      for (int j = 0; j < kQuads; ++j) {
+        const int i = base + 4 * (threadIdx.x + j * kThreads);
+        lv[j] = i + 3 < p.V ? __ldg(reinterpret_cast<const float4*>(row + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
 #pragma unroll
     for (int j = 0; j < kChunk / (4 * kThreads); ++j) {
       const int i = base + 4 * (threadIdx.x + j * kThreads);  // first token of this quad
@@ -110,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) sample_chunk_kernel(const SamplePara
                                                p.off_hi),
                                     p.seed_lo, p.seed_hi);
       if (p.vec4 && i + 3 < p.V) {
-        const float4 l = __ldg(reinterpret_cast<const float4*>(row + i));
+        const float4 l = lv[j];
         better_in_order(bk, bi, race_key(l.x, scale, w.x), i);
         better_in_order(bk, bi, race_key(l.y, scale, w.y), i + 1);
         better_in_order(bk, bi, race_key(l.z, scale, w.z), i + 2);
