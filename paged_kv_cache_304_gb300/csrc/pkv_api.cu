@@ -256,6 +256,19 @@ int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PKV_ERR_CUDA;
   }
+  CUtensorMap omap;
+  {
+    // out, same layout as q: boxes of 32 rows (one warp's rows) x 64 dims of
+    // one head, swizzled, for the bulk tensor stores of the epilogue.
+    cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
+    cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(num_q_heads) * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, 32};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  }
   CacheMaps maps;
   if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kPrefillTileTokens, 1, &maps))
     return PKV_ERR_CUDA;
@@ -274,7 +287,7 @@ int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv
   a.num_kv_heads = num_kv_heads;
   a.num_blocks = num_blocks;
   a.scale = scale;
-  cudaError_t e = launch_paged_attn_prefill(a, maps, qmap, sm_count(), static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_paged_attn_prefill(a, maps, qmap, omap, sm_count(), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -100,7 +100,8 @@ struct PrefillArgs {
   float scale;
 };
 cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv_maps,
-                                      const CUtensorMap& q_map, int num_sms, cudaStream_t stream);
+                                      const CUtensorMap& q_map, const CUtensorMap& out_map, int num_sms,
+                                      cudaStream_t stream);
 
 // ---- step metadata
 struct MetaArgs {

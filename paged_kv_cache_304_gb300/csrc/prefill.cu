@@ -33,8 +33,13 @@
 //   applies the causal mask on diagonal tiles, keeps the running row maximum
 //   (log2 units, scale * log2(e) folded in), waits for the previous P V of
 //   its slot, rescales O in tensor memory only when the maximum grew by
-//   more than 2^8, and stores P.  At the end it normalises O by the row sum,
-//   stages the bf16 rows in shared memory and writes whole rows.
+//   more than 2^8, and stores P.  At the end it normalises O by the row sum
+//   and stages the bf16 rows in the Q buffer in the layout of a TMA box; a
+//   warp whose 32 rows all belong to the sequence stores them with bulk
+//   tensor copies, a warp holding the sequence's end writes its rows with
+//   ordinary stores.
+// * Q and the first K tile are requested right after the barriers are set
+//   up, before the tensor-memory allocation and the block-wide barrier.
 // * Tiles are launched heaviest first (the last query tile of a sequence
 //   sees the most keys); the hardware block scheduler balances the rest.
 // Every wait is bounded (two seconds); on timeout the CTA flags
@@ -139,6 +144,18 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const CUten
 // tensor pipe, the limit.
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
+// Bulk tensor store of one box from shared memory, tracked by the bulk
+// async-group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // S = Q K^T: A = Q tile, B = K tile, both K-major (dims contiguous) with the
 // 128-byte swizzle; k-step kk selects 32 bytes of a 64-dim half.
 __device__ __forceinline__ void issue_s(uint32_t d, uint64_t qdesc, uint64_t kdesc) {
@@ -160,7 +177,8 @@ __device__ __forceinline__ void issue_pv(uint32_t o, uint32_t p_tmem, uint64_t v
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                   const PrefillParams p) {
   griddep_wait();
   griddep_launch_dependents();
   const int g = blockIdx.x / p.npairs;   // kv head
@@ -221,6 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.s_free[0], 4);
     mbar_init(&sm.s_free[1], 4);
     fence_barrier_init();
+    // Q and the first K tile go out before the tensor-memory allocation and
+    // the block-wide barrier (stage 0 starts empty, so no wait).
+    const int row0 = q0 + kTileM * m;
+    mbar_arrive_expect_tx(sm.q_full, has_b ? 2 * kTileBytes : kTileBytes);
+    tma_load_3d(sm.q, &qmap, sm.q_full, 0, hA, row0);
+    tma_load_3d(sm.q + kHalfBytes, &qmap, sm.q_full, 64, hA, row0);
+    if (has_b) {
+      tma_load_3d(sm.q + kTileBytes, &qmap, sm.q_full, 0, hA + 1, row0);
+      tma_load_3d(sm.q + kTileBytes + kHalfBytes, &qmap, sm.q_full, 64, hA + 1, row0);
+    }
+    mbar_arrive_expect_tx(&sm.k_full[0], kTileBytes);
+    load_kv_tile(p, &kmap, sm.k0, &sm.k_full[0], phys, 0, g);
   }
   if (warp == 1) {
     tc::alloc(sm.tmem_base, kTmemCols);
@@ -235,18 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const int row0 = q0 + kTileM * m;
-      mbar_arrive_expect_tx(sm.q_full, has_b ? 2 * kTileBytes : kTileBytes);
-      tma_load_3d(sm.q, &qmap, sm.q_full, 0, hA, row0);
-      tma_load_3d(sm.q + kHalfBytes, &qmap, sm.q_full, 64, hA, row0);
-      if (has_b) {
-        tma_load_3d(sm.q + kTileBytes, &qmap, sm.q_full, 0, hA + 1, row0);
-        tma_load_3d(sm.q + kTileBytes + kHalfBytes, &qmap, sm.q_full, 64, hA + 1, row0);
-      }
-      // Order K(0), K(1), V(0), K(2), V(1), ...: the MMA warp needs K(j+1)
-      // (for the next S) before V(j) (for this tile's P V).
+      // Order K(0) (already issued with Q), K(1), V(0), K(2), V(1), ...: the
+      // MMA warps need K(j+1) (for the next S) before V(j) (for P V of j).
       int phys_v = phys;  // block of the next V tile
-      for (int j = 0; j <= nkv; ++j) {
+      for (int j = 1; j <= nkv; ++j) {
         if (j < nkv) {
           if ((j & 1) == 0 && j > 0) {
             phys = nxt;
@@ -417,10 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after();
       const float inv = fast_rcp(l);
       // Stage the bf16 row in this slot's Q buffer (free: o_done implies
-      // every MMA of the CTA that reads Q has completed): 16-byte chunk c of
-      // row r goes to chunk c ^ (r % 16), so the 32 rows of a warp hit all
-      // banks.  Then the warp writes its 32 rows out two full rows per
-      // instruction instead of 32 scattered 16-byte pieces.
+      // every MMA of the CTA that reads Q has completed) in the layout of a
+      // TMA box: 64-dim halves 16 KiB apart, 128-byte rows, 16-byte chunk c
+      // of row r at chunk c ^ (r % 8).  A warp whose 32 rows all belong to
+      // the sequence stores them with two bulk tensor copies; otherwise it
+      // writes its rows that exist with ordinary stores.
       fence_proxy_async_smem();
       uint8_t* stage = sm.q + slot * kTileBytes;
 #pragma unroll
@@ -432,29 +455,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const float* v = o + 8 * c8;
-          const int c16 = 8 * hh + c8;
           uint4 w;
           w.x = pack_bf16x2(v[0] * inv, v[1] * inv);
           w.y = pack_bf16x2(v[2] * inv, v[3] * inv);
           w.z = pack_bf16x2(v[4] * inv, v[5] * inv);
           w.w = pack_bf16x2(v[6] * inv, v[7] * inv);
-          *reinterpret_cast<uint4*>(stage + r * 256 + ((c16 ^ (r & 15)) << 4)) = w;
+          *reinterpret_cast<uint4*>(stage + hh * kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) = w;
         }
       }
-      __syncwarp();
-      const int ch = lane & 15;
-      const int64_t row_stride = static_cast<int64_t>(p.Hq) * kHeadDim;  // elements between token rows
-      uint16_t* dst0 = p.out + static_cast<int64_t>(q0 + kTileM * m) * row_stride + h * kHeadDim + ch * 8;
       const int rows_left = n - kTileM * m;  // rows of this tile inside the sequence
+      if (32 * wq + 32 <= rows_left) {
+        fence_proxy_async_smem();  // the staged rows, before the async proxy reads them
+        __syncwarp();
+        if (lane == 0) {
+          const int row0 = q0 + kTileM * m + 32 * wq;
+          tma_store_3d(&omap, stage + wq * 32 * 128, 0, h, row0);
+          tma_store_3d(&omap, stage + kHalfBytes + wq * 32 * 128, 64, h, row0);
+          bulk_commit_and_wait_read();
+        }
+        __syncwarp();
+      } else {
+        __syncwarp();
+        const int ch = lane & 15;
+        const int64_t row_stride = static_cast<int64_t>(p.Hq) * kHeadDim;  // elements between token rows
+        uint16_t* dst0 = p.out + static_cast<int64_t>(q0 + kTileM * m) * row_stride + h * kHeadDim + ch * 8;
 #pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int tr = 32 * wq + 2 * i + (lane >> 4);  // tile row written by this lane
-        const uint4 w = *reinterpret_cast<const uint4*>(stage + tr * 256 + ((ch ^ (tr & 15)) << 4));
-        if (tr < rows_left) {
-          uint16_t* dst = dst0 + tr * row_stride;
-          asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
-                       "r"(w.w)
-                       : "memory");
+        for (int i = 0; i < 16; ++i) {
+          const int tr = 32 * wq + 2 * i + (lane >> 4);  // tile row written by this lane
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + (ch >> 3) * kHalfBytes + tr * 128 +
+                                                          (((ch & 7) ^ (tr & 7)) << 4));
+          if (tr < rows_left) {
+            uint16_t* dst = dst0 + tr * row_stride;
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
+                         "r"(w.w)
+                         : "memory");
+          }
         }
       }
     }
@@ -468,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv, const CUtensorMap& qmap,
-                                      int num_sms, cudaStream_t stream) {
+                                      const CUtensorMap& omap, int num_sms, cudaStream_t stream) {
   (void)num_sms;
   if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
   PrefillParams p;
@@ -491,7 +526,7 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
   if (e != cudaSuccess) return e;
   const int max_tiles = (a.max_seqlen_q + kTileM - 1) / kTileM;
   dim3 grid(a.num_kv_heads * p.npairs, a.num_seqs, max_tiles);
-  return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kv.k, kv.v, p);
+  return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, qmap, kv.k, kv.v, omap, p);
 }
 
 cudaError_t read_error_prefill(uint32_t* out, bool clear) {
