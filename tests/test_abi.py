@@ -88,3 +88,41 @@ def test_prefill_argument_errors(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(pkv.PkvLibraryError):
         pkv.load(str(tmp_path / "missing.so"))
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "pkv.h"
+
+/* A plain C caller of the library: the header is C, and the calls below
+   fail host-side validation (no device is touched). */
+int main(void) {
+  const void* fake = (const void*)0x1000;
+  int rc;
+  if (pkv_version() < 100) return 1;
+  if (!pkv_status_string(PKV_ERR_NULL)) return 2;
+  rc = pkv_kv_cache_write(NULL, 1024, fake, 1024, (const int32_t*)fake, 4, (pkv_bf16*)fake, (pkv_bf16*)fake, 4,
+                          256, 8, 128, NULL);
+  if (rc != PKV_ERR_NULL) return 3;
+  rc = pkv_paged_attn_prefill(fake, fake, fake, (const int32_t*)fake, (const int32_t*)fake, (const int32_t*)fake,
+                              8, 1, 16, 16, 16, 16, 8, 96, 256, 4, 0.088f, (pkv_bf16*)fake, NULL);
+  if (rc != PKV_ERR_UNSUPPORTED) return 4;
+  printf("ok %d\n", pkv_version());
+  return 0;
+}
+"""
+
+
+def test_plain_c_caller_links_and_runs(lib, tmp_path):
+    """The boundary works from C: compile a C99 program against include/pkv.h,
+    link it to libpkv.so and run it (argument-validation paths only)."""
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    libdir = os.path.dirname(LIB)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", inc, str(src), "-o", str(exe),
+                    "-L", libdir, "-lpkv", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
+    assert out.stdout.startswith("ok ")
