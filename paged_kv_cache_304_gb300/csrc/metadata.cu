@@ -9,7 +9,9 @@
 // prefill feeds only the tokens from num_cached_tokens on); "第六站：注意力层"
 // (the varlen calls take cumulative lengths).
 //
-// Two kernels, chained with programmatic dependent launch:
+// Up to 16384 sequences, one kernel does both steps (each CTA scans the
+// lengths itself); larger batches use two kernels, chained with
+// programmatic dependent launch:
 // * scan (one CTA): per sequence n_i = L_i - c_i new tokens; block-wide
 //   inclusive scans give cu_seqlens_q and cu_seqlens_k; context_lens = L.
 //   A sequence whose table is too short for L_i (the decode rule: a token at
@@ -157,6 +159,118 @@ __global__ void __launch_bounds__(256) metadata_fill_kernel(const MetaParams p) 
   }
 }
 
+// One kernel for batches of up to kFusedMaxSeqs sequences: every CTA scans
+// the lengths itself (into shared memory) and then fills its share of the
+// slots and table entries, so no second launch waits on a first.  CTA 0
+// writes the scanned arrays.
+constexpr int kFusedThreads = 256;
+constexpr int kFusedMaxSeqs = 16384;
+
+__global__ void __launch_bounds__(kFusedThreads) metadata_fused_kernel(const MetaParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ int cu_s[];  // [S + 1] cu_seqlens_q
+  __shared__ int warp_n[kFusedThreads / 32], warp_l[kFusedThreads / 32];
+  __shared__ int carry_n, carry_l;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool writer = blockIdx.x == 0;
+  if (tid == 0) {
+    carry_n = carry_l = 0;
+    cu_s[0] = 0;
+    if (writer) {
+      p.cu_q[0] = 0;
+      p.cu_k[0] = 0;
+    }
+  }
+  __syncthreads();
+  for (int base = 0; base < p.S; base += kFusedThreads) {
+    const int i = base + tid;
+    int n = 0, L = 0;
+    if (i < p.S) seq_counts(p, i, n, L);
+    int sn = n, sl = L;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yn = __shfl_up_sync(0xffffffffu, sn, o), yl = __shfl_up_sync(0xffffffffu, sl, o);
+      if (lane >= o) {
+        sn += yn;
+        sl += yl;
+      }
+    }
+    if (lane == 31) {
+      warp_n[wid] = sn;
+      warp_l[wid] = sl;
+    }
+    __syncthreads();
+    if (wid == 0) {
+      constexpr int kWarps = kFusedThreads / 32;
+      int wn = lane < kWarps ? warp_n[lane] : 0, wl = lane < kWarps ? warp_l[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < kWarps; o <<= 1) {
+        const int yn = __shfl_up_sync(0xffffffffu, wn, o), yl = __shfl_up_sync(0xffffffffu, wl, o);
+        if (lane >= o) {
+          wn += yn;
+          wl += yl;
+        }
+      }
+      if (lane < kWarps) {
+        warp_n[lane] = wn;
+        warp_l[lane] = wl;
+      }
+    }
+    __syncthreads();
+    const int off_n = carry_n + (wid ? warp_n[wid - 1] : 0);
+    const int off_l = carry_l + (wid ? warp_l[wid - 1] : 0);
+    if (i < p.S) {
+      cu_s[i + 1] = off_n + sn;
+      if (writer) {
+        p.cu_q[i + 1] = off_n + sn;
+        p.cu_k[i + 1] = off_l + sl;
+        p.ctx[i] = L;
+      }
+    }
+    __syncthreads();
+    if (tid == kFusedThreads - 1) {
+      carry_n = off_n + sn;
+      carry_l = off_l + sl;
+    }
+    __syncthreads();
+  }
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int total = cu_s[p.S];
+  if (t0 == 0 && total > p.token_capacity) atomicOr(&g_err_metadata, PKV_DEVERR_LEN_RANGE);
+  for (int64_t t = t0; t < p.token_capacity; t += nthreads) {
+    if (t >= total) {
+      p.slots[t] = -1;
+      continue;
+    }
+    int lo = 0, hi = p.S;  // find i with cu[i] <= t < cu[i+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu_s[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int i = lo;
+    const int c = __ldg(p.num_cached + i);
+    const int pos = c + static_cast<int>(t - cu_s[i]);
+    const int off = __ldg(p.table_offsets + i);
+    const int blk = __ldg(p.block_ids + off + pos / p.block_size);
+    if (blk < 0 || blk >= p.num_blocks) {
+      atomicOr(&g_err_metadata, PKV_DEVERR_BLOCK_RANGE);
+      p.slots[t] = -1;
+      continue;
+    }
+    p.slots[t] = blk * p.block_size + pos % p.block_size;
+  }
+  const int64_t entries = static_cast<int64_t>(p.S) * p.max_blocks;
+  for (int64_t e = t0; e < entries; e += nthreads) {
+    const int i = static_cast<int>(e / p.max_blocks);
+    const int k = static_cast<int>(e - static_cast<int64_t>(i) * p.max_blocks);
+    const int off = __ldg(p.table_offsets + i);
+    const int nb = __ldg(p.table_offsets + i + 1) - off;
+    p.tables[e] = k < nb ? __ldg(p.block_ids + off + k) : -1;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_prepare_metadata(const MetaArgs& a, int num_sms, cudaStream_t stream) {
@@ -175,13 +289,23 @@ cudaError_t launch_prepare_metadata(const MetaArgs& a, int num_sms, cudaStream_t
   p.ctx = a.context_lens;
   p.slots = a.slot_mapping;
   p.tables = a.block_tables;
-  cudaError_t e = launch_pdl(metadata_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
-  if (e != cudaSuccess) return e;
   const int64_t work = std::max<int64_t>(a.token_capacity, static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq);
   int64_t blocks = (work + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  if (a.num_seqs <= kFusedMaxSeqs) {
+    const size_t smem = (static_cast<size_t>(a.num_seqs) + 1) * sizeof(int);
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(metadata_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(metadata_fused_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFusedThreads), smem, stream,
+                      p);
+  }
+  cudaError_t e = launch_pdl(metadata_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
+  if (e != cudaSuccess) return e;
   return launch_pdl(metadata_fill_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 

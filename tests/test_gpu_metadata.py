@@ -71,6 +71,16 @@ def test_graph_padding_and_many_sequences():
     _check(tables, L - 1, L, 3, 20000, capacity=S + 37)
 
 
+def test_more_sequences_than_one_kernel_scans():
+    """Above 16384 sequences the scan and the fill run as two kernels."""
+    rng = np.random.default_rng(10)
+    S = 17000
+    L = rng.integers(1, 40, size=S)
+    perm = rng.permutation(S + 10)
+    tables = [[int(perm[i])] for i in range(S)]
+    _check(tables, L - 1, L, 1, S + 10, capacity=S + 5)
+
+
 def test_short_table_is_flagged_and_skipped():
     pkv.device_error(clear=True)
     got, _ = _run([[3], [5, 6]], [255, 0], [257, 300], 2, 8, capacity=300)
