@@ -13,7 +13,7 @@ working set (about 1.2 GB) is far larger than L2 and no flush is needed.
 Printed: one JSON line (rank 0).  `value` is the algorithmic HBM bytes of the
 whole step (decode K/V/q/out/metadata plus the KV write's reads and writes)
 divided by the step time.  `roofline` reports the dominant call
-(paged_attn_decode) against the measured HBM copy bandwidth.  Extra lines of
+(paged_attn_decode_fused_write) against the measured HBM copy bandwidth.  Extra lines of
 the same object report other workloads (graph-padded decode, 8B-shaped
 decode, prefill TFLOP/s, the 32768-token KV write).
 
