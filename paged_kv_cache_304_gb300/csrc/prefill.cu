@@ -79,7 +79,7 @@ struct Smem {
   uint8_t* q;   // 2 tiles
   uint8_t* k0;  // kKStages tiles
   uint8_t* v0;  // kVStages tiles
-  uint64_t* q_full;
+  uint64_t* q_full;   // [2 slots]
   uint64_t* k_full;   // [kKStages]
   uint64_t* k_empty;  // [kKStages]
   uint64_t* v_full;   // [kVStages]
@@ -99,7 +99,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.v0 = s.k0 + kKStages * kTileBytes;
   uint64_t* b = reinterpret_cast<uint64_t*>(s.v0 + kVStages * kTileBytes);
   s.q_full = b;
-  s.k_full = b + 1;
+  s.k_full = b + 2;
   s.k_empty = s.k_full + kKStages;
   s.v_full = s.k_empty + kKStages;
   s.v_empty = s.v_full + kVStages;
@@ -115,13 +115,16 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
 constexpr size_t kSmemBytes = 1024 + (2 + kKStages + kVStages) * kTileBytes + 32 * sizeof(uint64_t) + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
-__device__ __forceinline__ int load_block(const PrefillParams& p, int seq, int lb) {
-  int phys = __ldg(p.tables + static_cast<int64_t>(seq) * p.maxb + lb);
+__device__ __forceinline__ int checked_block(const PrefillParams& p, int phys) {
   if (phys < 0 || phys >= p.num_blocks) {
     atomicOr(&g_err_prefill, PKV_DEVERR_BLOCK_RANGE);
     phys = 0;
   }
   return phys;
+}
+
+__device__ __forceinline__ int load_block(const PrefillParams& p, int seq, int lb) {
+  return checked_block(p, __ldg(p.tables + static_cast<int64_t>(seq) * p.maxb + lb));
 }
 
 // One 128-token K or V tile (all 128 dims of kv head g) into `dst` as two
@@ -217,11 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    phys = load_block(p, seq, 0);
-    nxt = nkv > 2 ? load_block(p, seq, 1) : 0;
+    // Range-checked only after Q is requested: the check waits for the load.
+    phys = __ldg(p.tables + static_cast<int64_t>(seq) * p.maxb);
+    nxt = nkv > 2 ? __ldg(p.tables + static_cast<int64_t>(seq) * p.maxb + 1) : 0;
   }
   if (threadIdx.x == 0) {
-    mbar_init(sm.q_full, 1);
+    mbar_init(&sm.q_full[0], 1);
+    mbar_init(&sm.q_full[1], 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], has_b ? 2 : 1);  // released by each slot's S
@@ -242,15 +247,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q and the first K tile go out before the tensor-memory allocation and
     // the block-wide barrier (stage 0 starts empty, so no wait).
     const int row0 = q0 + kTileM * m;
-    mbar_arrive_expect_tx(sm.q_full, has_b ? 2 * kTileBytes : kTileBytes);
-    tma_load_3d(sm.q, &qmap, sm.q_full, 0, hA, row0);
-    tma_load_3d(sm.q + kHalfBytes, &qmap, sm.q_full, 64, hA, row0);
-    if (has_b) {
-      tma_load_3d(sm.q + kTileBytes, &qmap, sm.q_full, 0, hA + 1, row0);
-      tma_load_3d(sm.q + kTileBytes + kHalfBytes, &qmap, sm.q_full, 64, hA + 1, row0);
-    }
+    // Order Q_A, K(0), Q_B: slot A's first S needs only the first two.
+    mbar_arrive_expect_tx(&sm.q_full[0], kTileBytes);
+    tma_load_3d(sm.q, &qmap, &sm.q_full[0], 0, hA, row0);
+    tma_load_3d(sm.q + kHalfBytes, &qmap, &sm.q_full[0], 64, hA, row0);
+    phys = checked_block(p, phys);
     mbar_arrive_expect_tx(&sm.k_full[0], kTileBytes);
     load_kv_tile(p, &kmap, sm.k0, &sm.k_full[0], phys, 0, g);
+    if (has_b) {
+      mbar_arrive_expect_tx(&sm.q_full[1], kTileBytes);
+      tma_load_3d(sm.q + kTileBytes, &qmap, &sm.q_full[1], 0, hA + 1, row0);
+      tma_load_3d(sm.q + kTileBytes + kHalfBytes, &qmap, &sm.q_full[1], 64, hA + 1, row0);
+    }
+    nxt = checked_block(p, nxt);
   }
   if (warp == 1) {
     tc::alloc(sm.tmem_base, kTmemCols);
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The S columns are handed over S_A(0), S_B(0), S_A(1), ...: S_X(j)
       // waits for s_free[X] phase j - 1 (slot A) or j (slot B), completed
       // when the other slot (or, with one slot, this one) has read its S.
-      bool ok = mbar_wait(sm.q_full, 0, &g_err_prefill) && mbar_wait(&sm.k_full[0], 0, &g_err_prefill);
+      bool ok = mbar_wait(&sm.q_full[slot], 0, &g_err_prefill) && mbar_wait(&sm.k_full[0], 0, &g_err_prefill);
       if (ok && slot == 1) ok = mbar_wait(&sm.s_free[1], 0, &g_err_prefill);
       if (ok) {
         tc::fence_after();
