@@ -122,3 +122,25 @@ def test_prefill_repeat_is_deterministic():
     a = to_host(pkv.paged_attn_prefill(*args))
     b = to_host(pkv.paged_attn_prefill(*args))
     assert np.array_equal(a, b)
+
+
+def test_prefill_bad_block_ids_flag_without_fault():
+    """Block-table entries outside the pool (the first entry of one sequence,
+    the second of another) are read as block 0 and flagged in the device error
+    word; a sequence whose table is intact still matches the oracle."""
+    w = W.make_prefill("badblock", 815, [600, 300, 200], [0, 0, 0], 16, 8, num_blocks=8)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    okc, ovc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_cache_write(w.k_new, w.v_new, w.slot_mapping, okc, ovc)
+    tab = w.block_tables.copy()
+    tab[0, 0] = 1_000_000
+    tab[1, 1] = -5
+    pkv.device_error(clear=True)
+    out = pkv.paged_attn_prefill(to_dev(w.q), kc, vc, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(tab), w.scale,
+                                 int(np.diff(w.cu_seqlens_q).max()), w.max_seqlen_k)
+    torch.cuda.synchronize()
+    assert "BLOCK_RANGE" in pkv.device_error(clear=True)
+    rows = np.arange(w.cu_seqlens_q[2], w.cu_seqlens_q[3])
+    ref = oracle.paged_attn_prefill(w.q, okc, ovc, w.cu_seqlens_q, w.cu_seqlens_k, w.block_tables, w.scale, rows=rows)
+    check_close(to_host(out), ref, "intact sequence next to bad tables", rows=rows)
