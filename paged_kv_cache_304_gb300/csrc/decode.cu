@@ -524,13 +524,16 @@ __global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(cons
   if (pair >= p.B * p.Hq) return;
   const int b = pair / p.Hq, hq = pair - b * p.Hq;
   const int lane = threadIdx.x & 31;
-  const int L = clamp_len(__ldg(p.ctx + b), p.lmax);
+  // The length and the CTA range are requested together (the range is only
+  // read when the length is positive, i.e. when the decode kernel wrote it).
+  const int L_in = __ldg(p.ctx + b);
+  const int2 meta = p.ws_meta[b];
+  const int L = clamp_len(L_in, p.lmax);
   uint16_t* o = p.out + static_cast<int64_t>(pair) * kHeadDim + 4 * lane;
   if (L == 0) {
     *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
     return;
   }
-  const int2 meta = p.ws_meta[b];
   const int c0 = max(0, meta.x), c1 = min(grid - 1, meta.y);
   if (c1 <= c0) return;  // finished inside one CTA
   float M = -INFINITY;
