@@ -538,20 +538,58 @@ def _time_calls(torch, fn, reps: int, warm: int = 3, per_graph: int = 10):
         return statistics.median(x.elapsed_time(y) for x, y in times)
 
 
-def _decode_extra(torch, pkv, device, gen, w: W.DecodeWorkload, pk, reps=20):
+def _l2_evictor(torch, device):
+    """A callable that evicts L2 by reading a 256 MB buffer (a read leaves
+    clean lines; a write would leave dirty lines whose write-back would be
+    charged to whatever runs next)."""
+    src = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    dst = torch.empty(1, dtype=torch.float32, device=device)
+    return lambda: torch.sum(src, dim=0, keepdim=True, out=dst)
+
+
+def _time_cold(torch, fn, reps: int, evict):
+    """Median device time of one call of `fn` (replayed from a CUDA graph)
+    with L2 evicted before each rep; the eviction is outside the events."""
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        fn()
+    times = []
+    for _ in range(reps):
+        evict()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) for x, y in times)
+
+
+def _decode_extra(torch, pkv, device, gen, w: W.DecodeWorkload, pk, reps=20, cold_too=False):
     kv = make_cache(torch, 1, w.num_blocks, w.num_kv_heads, gen, device)
     q = torch.randn(w.q.shape, generator=gen, device=device).to(torch.bfloat16)
     ctx = torch.from_numpy(w.context_lens).to(device)
     tab = torch.from_numpy(w.block_tables).to(device)
     ws = pkv.decode_workspace(w.batch, w.num_q_heads, device)
     out = torch.empty_like(q)
-    ms = _time_calls(torch, lambda: pkv.paged_attn_decode(q, kv[0, 0], kv[1, 0], ctx, tab, w.scale, out=out,
-                                                          workspace=ws, max_context_len=w.max_context_len), reps)
+
+    def call():
+        pkv.paged_attn_decode(q, kv[0, 0], kv[1, 0], ctx, tab, w.scale, out=out, workspace=ws,
+                              max_context_len=w.max_context_len)
+    ms = _time_calls(torch, call, reps)
     nbytes = decode_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads)
     gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+           "bytes": nbytes}
+    if cold_too:
+        # back-to-back replays keep a small working set in L2; this is the
+        # latency of one call whose K/V must come from HBM
+        res["ms_cold_l2"] = round(_time_cold(torch, call, reps, _l2_evictor(torch, device)), 4)
     del kv
-    return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
-            "bytes": nbytes}
+    return res
 
 
 def _write_extra(torch, pkv, device, gen, w, pk, reps=20):
@@ -559,17 +597,8 @@ def _write_extra(torch, pkv, device, gen, w, pk, reps=20):
     k = torch.randn(w.k_new.shape, generator=gen, device=device).to(torch.bfloat16)
     v = torch.randn(w.v_new.shape, generator=gen, device=device).to(torch.bfloat16)
     slots = torch.from_numpy(w.slot_mapping).to(device)
-    # the write's own working set is about the size of L2: evict L2 between
-    # reps by reading a 256 MB buffer (a read leaves clean lines; a write would
-    # leave dirty lines whose write-back would be charged to the next rep)
-    flush_src = torch.ones(64 << 20, dtype=torch.float32, device=device)
-    flush_dst = torch.empty(1, dtype=torch.float32, device=device)
-
-    class _Flush:
-        @staticmethod
-        def fill_(_):
-            torch.sum(flush_src, dim=0, keepdim=True, out=flush_dst)
-    flush = _Flush()
+    # the write's own working set is about the size of L2: evict L2 between reps
+    evict = _l2_evictor(torch, device)
 
     def fn():
         pkv.kv_cache_write(k, v, slots, kv[0, 0], kv[1, 0])
@@ -579,7 +608,7 @@ def _write_extra(torch, pkv, device, gen, w, pk, reps=20):
     times = []
     stream = torch.cuda.current_stream()
     for _ in range(reps):
-        flush.fill_(1)
+        evict()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -655,7 +684,8 @@ def run_extras(torch, pkv, device, gen, pk):
     out["graph_padded_decode_b500_pad512"] = _decode_extra(torch, pkv, device, gen,
                                                             W.graph_padded_decode(fill_caches=False), pk)
     out["qwen3_8b_decode_b64"] = _decode_extra(torch, pkv, device, gen, W.qwen3_8b_decode(fill_caches=False), pk)
-    out["tiny_decode_b4_latency"] = _decode_extra(torch, pkv, device, gen, W.tiny_decode(fill_caches=False), pk)
+    out["tiny_decode_b4_latency"] = _decode_extra(torch, pkv, device, gen, W.tiny_decode(fill_caches=False), pk,
+                                                  cold_too=True)
     out["kv_write_qwen3_8b_prefill_32768_tokens"] = _write_extra(torch, pkv, device, gen,
                                                                  W.qwen3_8b_prefill(fill_caches=False), pk)
     out["chunked_prefill_prefix_budget16384"] = _prefill_extra(torch, pkv, device, gen,
@@ -699,7 +729,7 @@ def run_case(args, local):
         res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)
     elif args.case == "decode_tiny":
         w = W.tiny_decode(fill_caches=False)
-        res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)
+        res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps, cold_too=True)
     elif args.case == "sampler":
         res = _sampler_extra(torch, pkv, device, gen, pk, reps=reps)
         print(json.dumps({"case": args.case, "workload": "sampler_b256_vocab151936", "peak_kind": peak_kind, **res}),
