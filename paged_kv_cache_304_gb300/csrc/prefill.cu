@@ -39,7 +39,10 @@
 //   tensor copies, a warp holding the sequence's end writes its rows with
 //   ordinary stores.
 // * Q and the first K tile are requested right after the barriers are set
-//   up, before the tensor-memory allocation and the block-wide barrier.
+//   up, before the tensor-memory allocation and the block-wide barrier, in
+//   the order Q_A, K(0), Q_B with one Q barrier per slot, so slot A's first
+//   S waits for two tiles, not three; the first block-table entries are
+//   range-checked only after Q has been requested.
 // * Tiles are launched heaviest first (the last query tile of a sequence
 //   sees the most keys); the hardware block scheduler balances the rest.
 // Every wait is bounded (two seconds); on timeout the CTA flags
