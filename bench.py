@@ -90,6 +90,19 @@ def decode_bytes(ctx: np.ndarray, hq: int, hkv: int, d: int = 128, bs: int = 256
     return kv + qo + meta
 
 
+def decode_unique_bytes(ctx: np.ndarray, tables: np.ndarray, hq: int, hkv: int, d: int = 128,
+                        bs: int = 256) -> int:
+    """decode_bytes with every cache row counted once: a block that several
+    sequences share (a common prefix) is read from HBM once per call at best."""
+    used = {}
+    for b, L in enumerate(ctx.astype(np.int64)):
+        for lb in range(int((L + bs - 1) // bs)):
+            phys = int(tables[b, lb])
+            used[phys] = max(used.get(phys, 0), int(min(bs, L - bs * lb)))
+    kv = sum(used.values()) * hkv * d * 2 * 2
+    return kv + decode_bytes(ctx, hq, hkv, d, bs) - int(ctx.astype(np.int64).sum()) * hkv * d * 2 * 2
+
+
 def write_bytes(slots: np.ndarray, hkv: int, d: int = 128) -> int:
     """Algorithmic bytes of one KV write: K and V rows read and written for
     every non-padding token, plus the slot mapping."""
@@ -584,6 +597,10 @@ def _decode_extra(torch, pkv, device, gen, w: W.DecodeWorkload, pk, reps=20, col
     gbs = nbytes / (ms / 1e3) / 1e9
     res = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
            "bytes": nbytes}
+    ubytes = decode_unique_bytes(w.context_lens, w.block_tables, w.num_q_heads, w.num_kv_heads)
+    if ubytes != nbytes:
+        res["unique_bytes"] = ubytes
+        res["GB/s_unique"] = round(ubytes / (ms / 1e3) / 1e9, 1)
     if cold_too:
         # back-to-back replays keep a small working set in L2; this is the
         # latency of one call whose K/V must come from HBM
