@@ -131,3 +131,20 @@ def test_decode_scale_is_applied():
     w = W.make_decode("scale", 906, [500, 77], 16, 8, num_blocks=6)
     w.scale = 0.5 / math.sqrt(128)
     run_decode(w)
+
+
+def test_decode_understated_max_context_len_is_clamped_and_flagged():
+    """A context length above the stated max_context_len is read only up to
+    that bound and flagged; other sequences are unaffected."""
+    w = W.make_decode("understated", 906, [300, 1000], 16, 8, num_blocks=8)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    pkv.device_error(clear=True)
+    out = pkv.paged_attn_decode(to_dev(w.q), kc, vc, i32(w.context_lens), i32(w.block_tables), w.scale,
+                                max_context_len=512)
+    torch.cuda.synchronize()
+    assert "LEN_RANGE" in pkv.device_error(clear=True)
+    okc, ovc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_cache_write(w.k_new, w.v_new, w.slot_mapping, okc, ovc)
+    ref = oracle.paged_attn_decode(w.q, okc, ovc, w.context_lens, w.block_tables, w.scale)
+    check_close(to_host(out), ref, "sequence within the bound", rows=np.array([0]))

@@ -144,3 +144,16 @@ def test_prefill_bad_block_ids_flag_without_fault():
     rows = np.arange(w.cu_seqlens_q[2], w.cu_seqlens_q[3])
     ref = oracle.paged_attn_prefill(w.q, okc, ovc, w.cu_seqlens_q, w.cu_seqlens_k, w.block_tables, w.scale, rows=rows)
     check_close(to_host(out), ref, "intact sequence next to bad tables", rows=rows)
+
+
+def test_prefill_understated_max_seqlen_q_is_flagged():
+    """n_i above the stated max_seqlen_q: the launch covers too few query
+    tiles, which the kernel reports in the device error word (no fault)."""
+    w = W.make_prefill("understated", 816, [700, 90], [0, 0], 16, 8, num_blocks=6)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    pkv.device_error(clear=True)
+    pkv.paged_attn_prefill(to_dev(w.q), kc, vc, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables),
+                           w.scale, 128, w.max_seqlen_k)
+    torch.cuda.synchronize()
+    assert "LEN_RANGE" in pkv.device_error(clear=True)
