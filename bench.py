@@ -714,7 +714,7 @@ def run_extras(torch, pkv, device, gen, pk):
 
 
 CASES = ("step", "prefill_8b", "prefill_chunked", "decode_8b", "decode_padded", "decode_tiny", "write_32768",
-         "sampler")
+         "sampler", "metadata")
 
 
 def run_case(args, local):
@@ -752,6 +752,9 @@ def run_case(args, local):
         print(json.dumps({"case": args.case, "workload": "sampler_b256_vocab151936", "peak_kind": peak_kind, **res}),
               flush=True)
         return 0
+    elif args.case == "metadata":
+        w = W.qwen3_0p6b_decode(fill_caches=False)
+        res = _metadata_extra(torch, pkv, device, w, reps=reps)
     else:
         w = W.qwen3_8b_prefill(fill_caches=False)
         res = _write_extra(torch, pkv, device, gen, w, pk, reps=reps)
