@@ -252,6 +252,18 @@ def oracle_decode_layer_rate(min_seconds: float = 10.0, max_reps: int = 20):
     return gbs, oracle.num_threads(), desc
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu reports it (best effort)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 def step_config(w, world: int) -> dict:
     """The `config` of the benchmark step (the same for both arms)."""
     return {"workload": "qwen3_0.6b_decode_b256: 28 layers x paged_attn_decode_fused_write (KV write + decode)",
@@ -292,7 +304,7 @@ def run_reference(args, rank, world):
         "config": step_config(w, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": "each step: the KV write and decode of 32 of the 256 sequences of one of the "
-                                   "28 layers, GB/s of those algorithmic bytes"},
+                                   "28 layers, GB/s of those algorithmic bytes", "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -506,7 +518,7 @@ def run_pkv(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, desc = oracle_decode_layer_rate()
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, "cpu_model": cpu_model()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
