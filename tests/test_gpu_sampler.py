@@ -23,6 +23,10 @@ def _dev(a):
 
 def _compare(logits, temps, seed, offset):
     tok = pkv.sample_exponential_race(_dev(logits), _dev(temps), seed, offset).cpu().numpy()
+    return _check(tok, logits, temps, seed, offset)
+
+
+def _check(tok, logits, temps, seed, offset):
     ref, scores = oracle.default().sample(logits, temps, seed, offset, with_scores=True)
     diff = np.nonzero(tok != ref)[0]
     for b in diff:  # allowed only for a near-tie of the race scores
@@ -57,8 +61,8 @@ def test_strided_rows_and_repeatability():
     temps = _dev(np.full(20, 1.1, np.float32))
     a = pkv.sample_exponential_race(d, temps, 3, 4).cpu().numpy()
     b = pkv.sample_exponential_race(d, temps, 3, 4).cpu().numpy()
-    ref = oracle.default().sample(full[:, :2999], np.full(20, 1.1, np.float32), 3, 4)
-    assert np.array_equal(a, b) and (a == ref).mean() >= 0.95
+    assert np.array_equal(a, b)
+    _check(a, np.ascontiguousarray(full[:, :2999]), np.full(20, 1.1, np.float32), 3, 4)
 
 
 def test_distribution_chi_square():
