@@ -454,10 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every MMA of the CTA that reads Q has completed) in the layout of a
       // TMA box: 64-dim halves 16 KiB apart, 128-byte rows, 16-byte chunk c
       // of row r at chunk c ^ (r % 8).  A warp whose 32 rows all belong to
-      // the sequence stores them with two bulk tensor copies; otherwise it
-      // writes its rows that exist with ordinary stores.
+      // the sequence stores each 64-dim half with a bulk tensor copy as soon
+      // as it is staged; otherwise it writes its rows that exist with
+      // ordinary stores.
       fence_proxy_async_smem();
       uint8_t* stage = sm.q + slot * kTileBytes;
+      const int rows_left = n - kTileM * m;  // rows of this tile inside the sequence
+      const bool whole = 32 * wq + 32 <= rows_left;
+      const int row0 = q0 + kTileM * m + 32 * wq;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float o[64];
@@ -474,17 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           w.w = pack_bf16x2(v[6] * inv, v[7] * inv);
           *reinterpret_cast<uint4*>(stage + hh * kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) = w;
         }
-      }
-      const int rows_left = n - kTileM * m;  // rows of this tile inside the sequence
-      if (32 * wq + 32 <= rows_left) {
-        fence_proxy_async_smem();  // the staged rows, before the async proxy reads them
-        __syncwarp();
-        if (lane == 0) {
-          const int row0 = q0 + kTileM * m + 32 * wq;
-          tma_store_3d(&omap, stage + wq * 32 * 128, 0, h, row0);
-          tma_store_3d(&omap, stage + kHalfBytes + wq * 32 * 128, 64, h, row0);
-          bulk_commit_and_wait_read();
+        if (whole) {  // this half goes out while the next one is staged
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_3d(&omap, stage + hh * kHalfBytes + wq * 32 * 128, 64 * hh, h, row0);
         }
+      }
+      if (whole) {
+        if (lane == 0) bulk_commit_and_wait_read();
         __syncwarp();
       } else {
         __syncwarp();
