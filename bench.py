@@ -472,6 +472,19 @@ def run_pkv(args, rank, world, local):
         gms = timed(runner.graphs[B].replay)
         extra[name] = {"ms_per_step": round(gms, 4), "GB/s": round(step_bytes * world / (gms / 1e3) / 1e9, 2)}
         del runner
+    # the runner as a caller uses it: a real batch that is not a bucket size,
+    # copied into the static buffers and padded (slot -1, length 0) to the
+    # next bucket, then replayed
+    Bp = B - 6
+    runner = DecodeGraphRunner([(kv[0, l], kv[1, l]) for l in range(LAYERS)], hq, w.max_blocks_per_seq, w.scale,
+                               max_batch=B, max_context_len=maxctx, buckets=[Bp - Bp % 16, B], fused=True)
+    real = (qs[:, :Bp], ks[:, :Bp], vs[:, :Bp], slots[:Bp], ctx[:Bp], tab[:Bp])
+    rms = timed(lambda: runner.run(*real))
+    rbytes = LAYERS * (decode_bytes(w.context_lens[:Bp], hq, hkv) + write_bytes(w.slot_mapping[:Bp], hkv))
+    extra[f"decode_step_graph_runner_b{Bp}_bucket{B}"] = {
+        "ms_per_step": round(rms, 4), "GB/s": round(rbytes * world / (rms / 1e3) / 1e9, 2),
+        "note": "DecodeGraphRunner.run: input copies, pad rows and the replay of the fused 28-layer graph"}
+    del runner
     def unfused_step():
         for l in range(LAYERS):
             pkv.kv_cache_write(ks[l], vs[l], slots, kv[0, l], kv[1, l])
