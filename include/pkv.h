@@ -128,7 +128,9 @@ PKV_API size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
  *   context_lens  [batch] int32: L_b, the tokens of sequence b to attend to,
  *                 the new one included.  L_b == 0 marks a pad row: its output
  *                 is zeros and nothing is read for it.  L_b must be <=
- *                 max_context_len and <= max_blocks_per_seq * block_size.
+ *                 max_context_len and <= max_blocks_per_seq * block_size;
+ *                 a larger (or negative) L_b flags PKV_DEVERR_LEN_RANGE and
+ *                 is clamped to that bound (or to 0).
  *   block_tables  [batch, max_blocks_per_seq] int32, row b lists sequence b's
  *                 physical blocks in logical order; entries at index
  *                 >= ceil(L_b / block_size) are never read.
@@ -191,7 +193,12 @@ PKV_API int pkv_paged_attn_decode_fused_write(
  *                 sequence i sits at position c_i + j and attends to keys
  *                 0 .. c_i + j (causal mask aligned bottom-right).
  *   block_tables  [num_seqs, max_blocks_per_seq] int32.
- *   max_seqlen_q, max_seqlen_k  host-known upper bounds of n_i and L_i.
+ *   max_seqlen_q, max_seqlen_k  host-known upper bounds of n_i and L_i;
+ *                 max_seqlen_q sizes the launch (a sequence with more new
+ *                 tokens flags PKV_DEVERR_LEN_RANGE and its leading query
+ *                 tiles are not computed).  A sequence with c_i < 0 or
+ *                 L_i > max_blocks_per_seq * block_size flags the same bit
+ *                 and is skipped.
  *   out           [total_q, num_q_heads, head_dim] bf16.
  * Accumulation is fp32; probabilities are rounded to bf16 before the V
  * product.  total_q == 0 is a no-op.
