@@ -616,8 +616,8 @@ cudaError_t launch_paged_attn_decode(const DecodeArgs& a, const CacheMaps& maps,
   p.v_cache_w = reinterpret_cast<uint4*>(a.v_cache);
   const size_t smem = 1024 + kStages * p.stage_bytes + kQSlots * p.q_slot_bytes +
                       kStages * sizeof(TileHeader) + (2 * kStages + 2 * kQSlots) * sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = ensure_dyn_smem(decode_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_kernel, dim3(grid), dim3(32 * (a.num_kv_heads + 1)), smem, stream, maps.k, maps.v, p);
   if (e != cudaSuccess) return e;

@@ -297,8 +297,8 @@ cudaError_t launch_prepare_metadata(const MetaArgs& a, int num_sms, cudaStream_t
   if (a.num_seqs <= kFusedMaxSeqs) {
     const size_t smem = (static_cast<size_t>(a.num_seqs) + 1) * sizeof(int);
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(metadata_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+      static std::atomic<int> smem_set[kMaxDevices];
+      cudaError_t e = ensure_dyn_smem(metadata_fused_kernel, smem, smem_set);
       if (e != cudaSuccess) return e;
     }
     return launch_pdl(metadata_fused_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFusedThreads), smem, stream,

@@ -7,6 +7,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <utility>
 
 #include "pkv.h"
@@ -18,6 +19,27 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxKvHeads = 8;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxQHeads = 64;
+
+// Raise `kernel`'s dynamic shared-memory limit on the current device to at
+// least `bytes`, calling the runtime only when the request exceeds what was
+// already set on that device (`marks` holds one high-water mark per device,
+// zero-initialised static storage of the caller).
+constexpr int kMaxDevices = 64;
+template <typename... KArgs>
+cudaError_t ensure_dyn_smem(void (*kernel)(KArgs...), size_t bytes, std::atomic<int>* marks) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int want = static_cast<int>(bytes);
+  if (dev >= 0 && dev < kMaxDevices && want <= marks[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+    int cur = marks[dev].load(std::memory_order_relaxed);
+    while (cur < want && !marks[dev].compare_exchange_weak(cur, want, std::memory_order_release)) {
+    }
+  }
+  return e;
+}
 
 // Launch `kernel` on `stream` with programmatic stream serialization
 // allowed, so it may start while the previous kernel drains (each kernel

@@ -534,8 +534,8 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
   p.total_q = a.total_q;
   p.per_half = kv.per_head;
   p.sl2 = a.scale * 1.4426950408889634f;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = ensure_dyn_smem(prefill_kernel, kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const int max_tiles = (a.max_seqlen_q + kTileM - 1) / kTileM;
   dim3 grid(a.num_kv_heads * p.npairs, a.num_seqs, max_tiles);
