@@ -121,9 +121,14 @@ struct PrefillArgs {
   int32_t num_blocks;
   float scale;
 };
+// Stated max_seqlen_q up to which the persistent kernel is used (prefill.cu
+// dispatches; prefill_persistent.cu holds that kernel).
+constexpr int kPersistentMaxSeqlenQ = 2048;
 cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv_maps,
                                       const CUtensorMap& q_map, const CUtensorMap& out_map, int num_sms,
                                       cudaStream_t stream);
+cudaError_t launch_prefill_persistent(const PrefillArgs& a, const CacheMaps& kv_maps, const CUtensorMap& q_map,
+                                      const CUtensorMap& out_map, int num_sms, cudaStream_t stream);
 
 // ---- step metadata
 struct MetaArgs {
@@ -157,6 +162,7 @@ cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream);
 cudaError_t read_error_kv_write(uint32_t* out, bool clear);
 cudaError_t read_error_decode(uint32_t* out, bool clear);
 cudaError_t read_error_prefill(uint32_t* out, bool clear);
+cudaError_t read_error_prefill_persistent(uint32_t* out, bool clear);
 cudaError_t read_error_metadata(uint32_t* out, bool clear);
 cudaError_t read_error_sampler(uint32_t* out, bool clear);
 

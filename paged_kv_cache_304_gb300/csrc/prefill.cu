@@ -46,7 +46,13 @@
 // * Tiles are launched heaviest first (the last query tile of a sequence
 //   sees the most keys); the hardware block scheduler balances the rest.
 // Every wait is bounded (two seconds); on timeout the CTA flags
-// PKV_DEVERR_WAIT_TIMEOUT, frees its tensor memory and returns.
+// PKV_DEVERR_WAIT_TIMEOUT, lets the copies and MMAs it has already issued
+// complete (bounded waits on their barriers), frees its tensor memory and
+// returns.
+//
+// This grid form is used for long prompts (stated max_seqlen_q above 2048);
+// batches of short query tiles go to the persistent kernel in
+// prefill_persistent.cu, which computes the same tiles in the same order.
 #include <cuda_runtime.h>
 
 #include "pkv_device.cuh"
@@ -92,6 +98,7 @@ struct Smem {
   uint64_t* p_full;   // [2 slots]: P of this slot stored
   uint64_t* pv_done;  // [2 slots]: P V of this slot completed (P columns and O reusable)
   uint64_t* o_done;   // [2 slots]
+  uint64_t* drain;    // [2 slots]: every MMA of the slot's issuer completed (abort path)
   uint32_t* tmem_base;
 };
 
@@ -111,12 +118,22 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.p_full = s.s_free + 2;
   s.pv_done = s.p_full + 2;
   s.o_done = s.pv_done + 2;
-  s.tmem_base = reinterpret_cast<uint32_t*>(s.o_done + 2);
+  s.drain = s.o_done + 2;
+  s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 2);
   return s;
 }
 
 constexpr size_t kSmemBytes = 1024 + (2 + kKStages + kVStages) * kTileBytes + 32 * sizeof(uint64_t) + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
+
+// Wait used only after a timeout, to let work this CTA already issued (bulk
+// copies, MMAs) finish before its shared and tensor memory are given up:
+// bounded (100 ms), reports nothing (the timeout has been reported).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 100000000ull) return;
+}
 
 __device__ __forceinline__ int checked_block(const PrefillParams& p, int phys) {
   if (phys < 0 || phys >= p.num_blocks) {
@@ -243,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[i], 4);
       mbar_init(&sm.pv_done[i], 1);
       mbar_init(&sm.o_done[i], 1);
+      mbar_init(&sm.drain[i], 1);
     }
     mbar_init(&sm.s_free[0], 4);
     mbar_init(&sm.s_free[1], 4);
@@ -280,24 +298,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Order K(0) (already issued with Q), K(1), V(0), K(2), V(1), ...: the
       // MMA warps need K(j+1) (for the next S) before V(j) (for P V of j).
       int phys_v = phys;  // block of the next V tile
-      for (int j = 1; j <= nkv; ++j) {
+      int klast = 0, vlast = -1;  // last K and V tiles issued (K(0) went out with Q)
+      bool aborted = false;
+      for (int j = 1; j <= nkv && !aborted; ++j) {
         if (j < nkv) {
           if ((j & 1) == 0 && j > 0) {
             phys = nxt;
             if (2 * (j / 2 + 1) < nkv) nxt = load_block(p, seq, j / 2 + 1);
           }
           const int sk = j % kKStages;
-          if (!mbar_wait(&sm.k_empty[sk], ((j / kKStages) & 1) ^ 1, &g_err_prefill)) break;
+          if (!mbar_wait(&sm.k_empty[sk], ((j / kKStages) & 1) ^ 1, &g_err_prefill)) {
+            aborted = true;
+            break;
+          }
           mbar_arrive_expect_tx(&sm.k_full[sk], kTileBytes);
           load_kv_tile(p, &kmap, sm.k0 + sk * kTileBytes, &sm.k_full[sk], phys, (j & 1) * kTileN, g);
+          klast = j;
         }
         if (j > 0) {
           const int jv = j - 1, sv = jv % kVStages;
-          if (!mbar_wait(&sm.v_empty[sv], ((jv / kVStages) & 1) ^ 1, &g_err_prefill)) break;
+          if (!mbar_wait(&sm.v_empty[sv], ((jv / kVStages) & 1) ^ 1, &g_err_prefill)) {
+            aborted = true;
+            break;
+          }
           mbar_arrive_expect_tx(&sm.v_full[sv], kTileBytes);
           load_kv_tile(p, &vmap, sm.v0 + sv * kTileBytes, &sm.v_full[sv], phys_v, (jv & 1) * kTileN, g);
+          vlast = jv;
           if (jv & 1) phys_v = phys;  // V(jv + 1) starts the block K(j) is in
         }
+      }
+      if (aborted) {
+        // Let every copy already issued land before shared memory is given
+        // up: the last load of each stage, and both Q tiles.
+        for (int st = 0; st < kKStages; ++st) {
+          const int j = klast - (klast - st + kKStages) % kKStages;
+          if (j >= 0) drain_wait(&sm.k_full[st], (j / kKStages) & 1);
+        }
+        for (int st = 0; st < kVStages; ++st) {
+          const int j = vlast - (vlast - st + kVStages) % kVStages;
+          if (vlast >= 0 && j >= 0) drain_wait(&sm.v_full[st], (j / kVStages) & 1);
+        }
+        drain_wait(&sm.q_full[0], 0);
+        if (has_b) drain_wait(&sm.q_full[1], 0);
       }
     }
   } else if (warp == 1 || (warp == 10 && has_b)) {
@@ -328,20 +370,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = j + 1 < nkv;
         const int st1 = (j + 1) % kKStages;
         if (more) {
-          if (!mbar_wait(&sm.s_free[slot], (slot == 0 ? j : j + 1) & 1, &g_err_prefill)) break;
-          if (!mbar_wait(&sm.k_full[st1], ((j + 1) / kKStages) & 1, &g_err_prefill)) break;
+          if (!mbar_wait(&sm.s_free[slot], (slot == 0 ? j : j + 1) & 1, &g_err_prefill) ||
+              !mbar_wait(&sm.k_full[st1], ((j + 1) / kKStages) & 1, &g_err_prefill)) {
+            ok = false;
+            break;
+          }
           tc::fence_after();
           issue_s(sT, qd, desc_add(kd0, st1 * kTileBytes));
           tc::commit(&sm.s_full[slot]);
           tc::commit(&sm.k_empty[st1]);
         }
-        if (!mbar_wait(&sm.p_full[slot], j & 1, &g_err_prefill)) break;
-        if (!mbar_wait(&sm.v_full[sv], (j / kVStages) & 1, &g_err_prefill)) break;
+        if (!mbar_wait(&sm.p_full[slot], j & 1, &g_err_prefill) ||
+            !mbar_wait(&sm.v_full[sv], (j / kVStages) & 1, &g_err_prefill)) {
+          ok = false;
+          break;
+        }
         tc::fence_after();
         issue_pv(oX, pX, desc_add(vd0, sv * kTileBytes), j > 0);
         tc::commit(&sm.pv_done[slot]);
         if (!more) tc::commit(&sm.o_done[slot]);
         tc::commit(&sm.v_empty[sv]);
+      }
+      if (!ok) {
+        // A wait gave up: every MMA this thread issued has completed once
+        // this commit arrives, so tensor memory can be freed after it.
+        tc::commit(&sm.drain[slot]);
+        drain_wait(&sm.drain[slot], 0);
       }
     }
   } else if (warp >= 2 && warp < 10 && (warp < 6 || has_b)) {
@@ -517,8 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv, const CUtensorMap& qmap,
                                       const CUtensorMap& omap, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
   if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
+  // Short query tiles: a CTA launch per 128-row tile costs about as much as
+  // the tile's tensor work, so they go to the persistent kernel.
+  if (a.max_seqlen_q <= kPersistentMaxSeqlenQ) return launch_prefill_persistent(a, kv, qmap, omap, num_sms, stream);
   PrefillParams p;
   p.cu_q = a.cu_seqlens_q;
   p.cu_k = a.cu_seqlens_k;
@@ -544,9 +600,12 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
 
 cudaError_t read_error_prefill(uint32_t* out, bool clear) {
   unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_err_prefill, sizeof v);
+  uint32_t vp = 0;
+  cudaError_t e = read_error_prefill_persistent(&vp, clear);
   if (e != cudaSuccess) return e;
-  *out = v;
+  e = cudaMemcpyFromSymbol(&v, g_err_prefill, sizeof v);
+  if (e != cudaSuccess) return e;
+  *out = v | vp;
   if (clear) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_err_prefill, &zero, sizeof zero);

@@ -3,8 +3,14 @@
 Each case writes the step's new tokens with the library's KV write (checked
 bit-exact), runs prefill through the C ABI and compares with the oracle:
 every output element at sizes the oracle finishes quickly, sampled rows (the
-first and last rows of every sequence plus a seeded sample) at the
-8B-shaped 4 x 8192 size.  Bar: max-abs <= 2e-2, mean-abs <= 2e-3.
+first and last rows of every query tile plus 1024 seeded rows per sequence)
+at the 8B-shaped 4 x 8192 size.  Bar: max-abs <= 2e-2, mean-abs <= 2e-3.
+
+The library has two prefill kernels, chosen by the stated max_seqlen_q: a
+persistent one for batches of short query tiles (<= 2048, e.g. the chunked
+16384-token step and every edge case here) and one CTA per query tile above
+that (4 x 8192).  Both are checked against the oracle, and against each other
+bit for bit on the same inputs.
 """
 
 import math
@@ -46,15 +52,31 @@ def test_prefill_chunked_prefix_budget16384():
     run_prefill(W.chunked_prefill_prefix())
 
 
-def test_prefill_qwen3_8b_4x8192_sampled_rows():
-    w = W.qwen3_8b_prefill()
+def config5_rows(w: W.PrefillWorkload) -> np.ndarray:
+    """Rows checked at 4 x 8192: the first and last row of every 128-row query
+    tile of every sequence (so every query tile a CTA can own is covered),
+    plus 1024 distinct seeded rows per sequence (about 4550 rows in all)."""
     rng = np.random.default_rng(8192)
     rows = []
     for i in range(w.num_seqs):
         lo, hi = int(w.cu_seqlens_q[i]), int(w.cu_seqlens_q[i + 1])
-        rows += [lo, lo + 1, lo + 127, lo + 128, hi - 129, hi - 1]
-        rows += list(rng.integers(lo, hi, size=26))
-    run_prefill(w, rows=np.unique(np.array(rows)))
+        starts = np.arange(lo, hi, 128)
+        rows += list(starts) + list(np.minimum(starts + 127, hi - 1))
+        rows += list(rng.choice(np.arange(lo, hi), size=min(1024, hi - lo), replace=False))
+    return np.unique(np.array(rows))
+
+
+def test_prefill_qwen3_8b_4x8192_sampled_rows():
+    """Every query tile's first and last rows plus 1024 seeded rows per
+    sequence; the fp64 oracle takes about half a minute on 8-16 host cores."""
+    w = W.qwen3_8b_prefill()
+    rows = config5_rows(w)
+    tiles = set()
+    for r in rows:
+        i = int(np.searchsorted(w.cu_seqlens_q, r, side="right")) - 1
+        tiles.add((i, (int(r) - int(w.cu_seqlens_q[i])) // 128))
+    assert len(tiles) == sum(-(-int(n) // 128) for n in w.seqlens_q)
+    run_prefill(w, rows=rows)
 
 
 EDGE = [
@@ -155,5 +177,50 @@ def test_prefill_understated_max_seqlen_q_is_flagged():
     pkv.device_error(clear=True)
     pkv.paged_attn_prefill(to_dev(w.q), kc, vc, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables),
                            w.scale, 128, w.max_seqlen_k)
+    torch.cuda.synchronize()
+    assert "LEN_RANGE" in pkv.device_error(clear=True)
+
+
+def _prefill_both_kernels(w: W.PrefillWorkload):
+    """Run one workload through the persistent kernel (stated max_seqlen_q at
+    most 2048) and through the one-CTA-per-tile kernel (the same call with
+    max_seqlen_q overstated to 4096, a legal upper bound)."""
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    args = (to_dev(w.q), kc, vc, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables), w.scale)
+    a = to_host(pkv.paged_attn_prefill(*args, w.max_seqlen_q, w.max_seqlen_k))
+    b = to_host(pkv.paged_attn_prefill(*args, 4096, max(4096, w.max_seqlen_k)))
+    torch.cuda.synchronize()
+    assert pkv.device_error() == []
+    return a, b
+
+
+@pytest.mark.parametrize("case", ["chunked", "edges", "groups12_4", "groups16_1"])
+def test_prefill_persistent_and_grid_kernels_bit_identical(case):
+    """Both prefill kernels compute every tile with the same steps in the same
+    order: their outputs agree bit for bit (and the persistent one matches the
+    oracle in the tests above)."""
+    if case == "chunked":
+        w = W.chunked_prefill_prefix()
+    elif case == "edges":
+        w = W.make_prefill("both_edges", 821, [1, 127, 129, 300, 1025, 40], [0, 0, 1, 255, 896, 0], 16, 8,
+                           num_blocks=16)
+    elif case == "groups12_4":
+        w = W.make_prefill("both_g3", 822, [700, 130, 1], [300, 0, 0], 12, 4, num_blocks=10)
+    else:
+        w = W.make_prefill("both_g16", 823, [900, 257], [0, 100], 16, 1, num_blocks=10)
+    a, b = _prefill_both_kernels(w)
+    assert np.array_equal(a, b), "persistent and grid prefill kernels differ"
+
+
+def test_prefill_understated_max_seqlen_q_long_prompt_is_flagged():
+    """Above 2048 stated query tokens the one-CTA-per-tile kernel runs; a
+    sequence longer than the stated bound is flagged there too (no fault)."""
+    w = W.make_prefill("understated_long", 817, [2600, 300], [0, 0], 16, 8, num_blocks=14)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    pkv.device_error(clear=True)
+    pkv.paged_attn_prefill(to_dev(w.q), kc, vc, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables),
+                           w.scale, 2100, w.max_seqlen_k)
     torch.cuda.synchronize()
     assert "LEN_RANGE" in pkv.device_error(clear=True)
