@@ -36,8 +36,9 @@
  *   num_kv_heads with group size num_q_heads / num_kv_heads in [1, 16], and
  *   num_q_heads <= 64.  Other shapes return PKV_ERR_UNSUPPORTED.
  * - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
- * - Return value: PKV_OK, or a negative pkv_status for a host-side argument
- *   error (nothing is launched) or a launch error.  Faults inside a kernel
+ * - Return value (pkv_status, an int-sized enum): PKV_OK, or a negative
+ *   status for a host-side argument error (nothing is launched) or a launch
+ *   error.  Faults inside a kernel
  *   surface at the caller's next synchronisation.  Invalid device-side values
  *   that the host cannot see (an out-of-range slot or block id, a bounded wait
  *   that timed out) never fault: the offending access is skipped or clamped
@@ -106,16 +107,23 @@ PKV_API int pkv_version(void);
  * Pointers and strides must give 16-byte aligned rows (PKV_ERR_ALIGN
  * otherwise).  num_tokens == 0 is a no-op.
  */
-PKV_API int pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16* v,
+PKV_API pkv_status pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16* v,
                        int64_t v_token_stride, const int32_t* slot_mapping, int32_t num_tokens,
                        pkv_bf16* k_cache, pkv_bf16* v_cache, int32_t num_blocks, int32_t block_size,
                        int32_t num_kv_heads, int32_t head_dim, void* stream);
 
 /*
- * Scratch bytes pkv_paged_attn_decode needs for `batch` sequences on the
- * current CUDA device (it depends on the device's SM count).
+ * Scratch bytes pkv_paged_attn_decode (and the fused-write variant) needs for
+ * `batch` sequences on the CUDA device that is current when this is called.
+ * The size depends on that device's SM count (the decode kernel splits the
+ * batch's tokens into one equal share per SM and keeps one partial result
+ * per (sequence or share boundary, query head)), so query it with the device
+ * the decode will run on current.  `max_context_len` is accepted so that the
+ * query takes the decode call's own bounds; the size does not depend on it.
+ * Returns 0 for a negative batch, num_q_heads <= 0, or when the device cannot
+ * be queried.
  */
-PKV_API size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim);
+PKV_API size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t max_context_len);
 
 /*
  * Decode attention (page section "第六站：注意力层": decode attends from one
@@ -140,12 +148,12 @@ PKV_API size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
  *                 K, V the kv head h / (num_q_heads/num_kv_heads) rows of the
  *                 first L_b logical positions.  Accumulation is fp32; the
  *                 probabilities are rounded to bf16 before the V product.
- *   workspace     >= pkv_decode_workspace_bytes(batch, num_q_heads, head_dim)
+ *   workspace     >= pkv_decode_workspace_bytes(batch, num_q_heads, max_context_len)
  *                 device bytes, 256-byte aligned, contents need not be
  *                 initialised; overwritten by the call.  Two calls that may
  *                 run concurrently need two workspaces.
  */
-PKV_API int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+PKV_API pkv_status pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
                           const int32_t* context_lens, const int32_t* block_tables,
                           int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
@@ -169,7 +177,7 @@ PKV_API int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, co
  *   k_cache, v_cache  written at those slots, read as in pkv_paged_attn_decode.
  * Every other argument is as in pkv_paged_attn_decode.
  */
-PKV_API int pkv_paged_attn_decode_fused_write(
+PKV_API pkv_status pkv_paged_attn_decode_fused_write(
     const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride, const pkv_bf16* v_new,
     int64_t v_token_stride, const int32_t* slot_mapping, pkv_bf16* k_cache, pkv_bf16* v_cache,
     const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -203,7 +211,7 @@ PKV_API int pkv_paged_attn_decode_fused_write(
  * Accumulation is fp32; probabilities are rounded to bf16 before the V
  * product.  total_q == 0 is a no-op.
  */
-PKV_API int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+PKV_API pkv_status pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                            int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
@@ -224,20 +232,23 @@ PKV_API int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, c
  * Scratch lives in one fixed array inside the library, PKV_DECODE_STATIC_SCRATCH_BYTES
  * (8 MiB) per GPU, held by every GPU that loads the library until the process
  * exits.  A call whose batch needs more than that
- * (pkv_decode_workspace_bytes(batch, num_q_heads, head_dim) > 8 MiB, e.g.
+ * (pkv_decode_workspace_bytes(batch, num_q_heads, max_context_len) > 8 MiB, e.g.
  * batch above 855 at 16 query heads on a 152-SM GPU) returns PKV_ERR_WORKSPACE
  * and launches nothing.  The call allocates nothing and frees nothing.
  *
  * The first call on a device looks up that array's device address (with the
  * device current) and caches it; make that first call before any stream
- * capture.  Every call on a device shares the one array and it keeps the
+ * capture (a first call made while `stream` is being captured returns
+ * PKV_ERR_CUDA and leaves the capture untouched).  The cached address belongs
+ * to the device's primary context as it was at that first call: resetting
+ * the device (cudaDeviceReset) afterwards is not supported by this call.  Every call on a device shares the one array and it keeps the
  * previous call's contents; no part of it needs to start at zero.  Calls
  * that can overlap on the GPU (different streams without ordering between
  * them) race on the array and give undefined results: order them, or use
  * pkv_paged_attn_decode with one workspace per stream.
  */
 #define PKV_DECODE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
-PKV_API int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache,
+PKV_API pkv_status pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache,
                                           const pkv_bf16* v_cache, const int32_t* context_lens,
                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
                                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -270,7 +281,7 @@ PKV_API int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_c
  * new block) or whose lengths are inconsistent contributes no tokens and
  * flags PKV_DEVERR_LEN_RANGE; more tokens than token_capacity also flag it.
  */
-PKV_API int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets,
+PKV_API pkv_status pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets,
                                  const int32_t* num_cached, const int32_t* seq_lens, int32_t num_seqs,
                                  int32_t token_capacity, int32_t max_blocks_per_seq, int32_t block_size,
                                  int32_t num_blocks, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
@@ -298,7 +309,7 @@ PKV_API int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_
  *                 aligned, need not be initialised.
  */
 PKV_API size_t pkv_sample_workspace_bytes(int32_t batch, int32_t vocab);
-PKV_API int pkv_sample_exponential_race(const float* logits, int64_t row_stride, const float* temperatures,
+PKV_API pkv_status pkv_sample_exponential_race(const float* logits, int64_t row_stride, const float* temperatures,
                                         int32_t batch, int32_t vocab, uint64_t seed, uint64_t offset,
                                         int32_t* out_tokens, void* workspace, size_t workspace_bytes,
                                         void* stream);
@@ -308,7 +319,7 @@ PKV_API int pkv_sample_exponential_race(const float* logits, int64_t row_stride,
  * current device.  Synchronises the device.  *out receives an OR of
  * PKV_DEVERR_* bits set by kernels since the last clear.
  */
-PKV_API int pkv_device_error(uint32_t* out, int clear);
+PKV_API pkv_status pkv_device_error(uint32_t* out, int clear);
 
 #ifdef __cplusplus
 }

@@ -141,14 +141,16 @@ def kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
         slot_mapping.data_ptr(), n, k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d, _stream(k_cache)))
 
 
-def decode_workspace_bytes(batch: int, num_q_heads: int, head_dim: int = 128) -> int:
-    return int(load().pkv_decode_workspace_bytes(batch, num_q_heads, head_dim))
+def decode_workspace_bytes(batch: int, num_q_heads: int, max_context_len: int = 0) -> int:
+    """Scratch bytes of paged_attn_decode on the current device (depends on its SM count)."""
+    return int(load().pkv_decode_workspace_bytes(batch, num_q_heads, max_context_len))
 
 
-def decode_workspace(batch: int, num_q_heads: int, device, head_dim: int = 128) -> torch.Tensor:
+def decode_workspace(batch: int, num_q_heads: int, device, max_context_len: int = 0) -> torch.Tensor:
     """A workspace tensor for paged_attn_decode (uninitialised bytes)."""
-    return torch.empty(max(256, decode_workspace_bytes(batch, num_q_heads, head_dim)), dtype=torch.uint8,
-                       device=device)
+    with torch.cuda.device(device):
+        n = decode_workspace_bytes(batch, num_q_heads, max_context_len)
+    return torch.empty(max(256, n), dtype=torch.uint8, device=device)
 
 
 def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, context_lens: torch.Tensor,
@@ -177,7 +179,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
     if workspace is None:
-        workspace = decode_workspace(B, hq, q.device, d)
+        workspace = decode_workspace(B, hq, q.device)
     maxb = int(block_tables.shape[1])
     if max_context_len is None:
         max_context_len = maxb * bs
@@ -216,7 +218,7 @@ def paged_attn_decode_fused_write(q: torch.Tensor, k_new: torch.Tensor, v_new: t
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        workspace = decode_workspace(B, hq, q.device, d)
+        workspace = decode_workspace(B, hq, q.device)
     maxb = int(block_tables.shape[1])
     if max_context_len is None:
         max_context_len = maxb * bs

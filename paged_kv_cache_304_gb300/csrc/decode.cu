@@ -126,6 +126,15 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const DecodeParams& p) {
 }
 
 // ------------------------------------------------------------------ producer
+// Wait used only after a timeout, to let copies this CTA already issued land
+// before its shared memory is given up: bounded (100 ms), reports nothing
+// (the timeout has been reported).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 100000000ull) return;
+}
+
 struct ProducerState {
   uint32_t it = 0;     // tiles issued
   uint32_t units = 0;  // units started
@@ -310,6 +319,15 @@ __device__ void producer(const DecodeParams& p, const Smem& sm, const CUtensorMa
       sm.hdr[stage].b = -1;
       mbar_arrive(&sm.full[stage]);
     }
+  }
+  if (lane == 0 && !ps.ok) {
+    // A wait gave up: let the copies already issued into the ring and the
+    // query slots land (bounded waits on their barriers) before the CTA
+    // exits and its shared memory is handed to another CTA.
+    for (uint32_t i = ps.it > kStages ? ps.it - kStages : 0; i < ps.it; ++i)
+      drain_wait(&sm.full[i % kStages], (i / kStages) & 1u);
+    for (uint32_t u = ps.units > kQSlots ? ps.units - kQSlots : 0; u < ps.units; ++u)
+      drain_wait(&sm.qfull[u % kQSlots], (u / kQSlots) & 1u);
   }
 }
 

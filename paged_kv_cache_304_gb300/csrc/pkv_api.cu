@@ -85,7 +85,7 @@ bool encode_cache_maps(const void* k_cache, const void* v_cache, int num_blocks,
 }
 
 // Shape checks shared by the two attention calls.
-int check_attn_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+pkv_status check_attn_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                      int32_t num_blocks, int32_t max_blocks_per_seq, float scale) {
   if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0)
@@ -121,7 +121,7 @@ const char* pkv_status_string(int status) {
 
 int pkv_version(void) { return 100; }
 
-int pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16* v, int64_t v_token_stride,
+pkv_status pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16* v, int64_t v_token_stride,
                        const int32_t* slot_mapping, int32_t num_tokens, pkv_bf16* k_cache, pkv_bf16* v_cache,
                        int32_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                        void* stream) {
@@ -140,8 +140,8 @@ int pkv_kv_cache_write(const pkv_bf16* k, int64_t k_token_stride, const pkv_bf16
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim) {
-  (void)head_dim;
+size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t max_context_len) {
+  (void)max_context_len;  // the partials' size does not depend on the lengths
   if (batch < 0 || num_q_heads <= 0) return 0;
   const int sms = sm_count();
   if (sms <= 0) return 0;
@@ -153,13 +153,13 @@ size_t pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t he
 namespace {
 
 // Shared by the plain and the fused-write decode entry points.
-int decode_common(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache, const int32_t* context_lens,
+pkv_status decode_common(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache, const int32_t* context_lens,
                   const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
                   int32_t max_context_len, float scale, pkv_bf16* out, void* workspace, size_t workspace_bytes,
                   void* stream, DecodeArgs& a) {
   if (batch < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
-  int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  const pkv_status st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
   if (st != PKV_OK) return st;
   if (max_context_len >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
@@ -192,7 +192,7 @@ int decode_common(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_
 
 extern "C" {
 
-int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+pkv_status pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
                           const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks_per_seq,
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
@@ -203,7 +203,7 @@ int pkv_paged_attn_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_
                        workspace_bytes, stream, a);
 }
 
-int pkv_paged_attn_decode_fused_write(const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride,
+pkv_status pkv_paged_attn_decode_fused_write(const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride,
                                       const pkv_bf16* v_new, int64_t v_token_stride, const int32_t* slot_mapping,
                                       pkv_bf16* k_cache, pkv_bf16* v_cache, const int32_t* context_lens,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch,
@@ -229,13 +229,13 @@ int pkv_paged_attn_decode_fused_write(const pkv_bf16* q, const pkv_bf16* k_new, 
                        workspace_bytes, stream, a);
 }
 
-int pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+pkv_status pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_tables,
                            int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
                            int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t block_size, int32_t num_blocks, float scale, pkv_bf16* out, void* stream) {
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PKV_ERR_SHAPE;
-  int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  const pkv_status st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
   if (st != PKV_OK) return st;
   if (max_seqlen_q > max_seqlen_k) return PKV_ERR_SHAPE;
   if (num_seqs > 65535 || max_seqlen_q > (1 << 22) || max_seqlen_k >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
@@ -312,12 +312,18 @@ std::mutex g_static_scratch_mutex;
 void* g_static_scratch_ptr[kMaxDevicesCached] = {};
 
 // Device address of the fixed scratch on the current device, looked up once
-// per device (with that device current) and cached.  nullptr on failure.
-void* static_scratch_for_current_device() {
+// per device (with that device current) and cached.  nullptr on failure, and
+// also when the lookup would have to happen while `stream` is being captured
+// into a CUDA graph: the lookup may load the library's device code, which is
+// not something to do inside a capture, so the first call on a device must
+// come before any capture (the header says so).
+void* static_scratch_for_current_device(cudaStream_t stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached) return nullptr;
   std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
   if (!g_static_scratch_ptr[dev]) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_decode_static_scratch) != cudaSuccess) return nullptr;
     g_static_scratch_ptr[dev] = ptr;
@@ -330,13 +336,13 @@ void* static_scratch_for_current_device() {
 
 extern "C" {
 
-int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+pkv_status pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
                                   const int32_t* context_lens, const int32_t* block_tables,
                                   int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
                                   int32_t max_context_len, float scale, pkv_bf16* out, void* stream) {
   if (batch < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
-  int st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  const pkv_status st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
   if (st != PKV_OK) return st;
   if (max_context_len >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
@@ -345,7 +351,7 @@ int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, co
   // Reject batches whose partials do not fit the fixed array, before launching.
   const size_t need = decode_workspace_bytes(batch, num_q_heads, sms);
   if (need > PKV_DECODE_STATIC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
-  void* scratch = static_scratch_for_current_device();
+  void* scratch = static_scratch_for_current_device(static_cast<cudaStream_t>(stream));
   if (!scratch) return PKV_ERR_CUDA;
   // Nothing in the scratch must start at zero: every partial and every
   // per-sequence record the combine step reads is written earlier in the
@@ -355,7 +361,7 @@ int pkv_paged_attn_decode_noalloc(const pkv_bf16* q, const pkv_bf16* k_cache, co
                                out, scratch, PKV_DECODE_STATIC_SCRATCH_BYTES, stream);
 }
 
-int pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets, const int32_t* num_cached,
+pkv_status pkv_prepare_metadata(const int32_t* block_ids, const int32_t* table_offsets, const int32_t* num_cached,
                          const int32_t* seq_lens, int32_t num_seqs, int32_t token_capacity,
                          int32_t max_blocks_per_seq, int32_t block_size, int32_t num_blocks, int32_t* cu_seqlens_q,
                          int32_t* cu_seqlens_k, int32_t* context_lens, int32_t* slot_mapping, int32_t* block_tables,
@@ -393,7 +399,7 @@ size_t pkv_sample_workspace_bytes(int32_t batch, int32_t vocab) {
   return sample_workspace_bytes(batch, vocab);
 }
 
-int pkv_sample_exponential_race(const float* logits, int64_t row_stride, const float* temperatures, int32_t batch,
+pkv_status pkv_sample_exponential_race(const float* logits, int64_t row_stride, const float* temperatures, int32_t batch,
                                 int32_t vocab, uint64_t seed, uint64_t offset, int32_t* out_tokens, void* workspace,
                                 size_t workspace_bytes, void* stream) {
   if (batch < 0 || vocab <= 0 || row_stride < vocab) return PKV_ERR_SHAPE;
@@ -416,7 +422,7 @@ int pkv_sample_exponential_race(const float* logits, int64_t row_stride, const f
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-int pkv_device_error(uint32_t* out, int clear) {
+pkv_status pkv_device_error(uint32_t* out, int clear) {
   if (!out) return PKV_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
   uint32_t a = 0, b = 0, c = 0, d = 0;

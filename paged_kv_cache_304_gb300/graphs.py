@@ -87,7 +87,7 @@ class DecodeGraphRunner:
             ctx=torch.zeros((max_batch,), dtype=torch.int32, device=dev),
             tables=torch.full((max_batch, max_blocks_per_seq), -1, dtype=torch.int32, device=dev),
         )
-        self.workspace = decode_workspace(max_batch, num_q_heads, dev, d)
+        self.workspace = decode_workspace(max_batch, num_q_heads, dev)
         self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
         self._capture()
 

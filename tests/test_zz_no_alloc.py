@@ -79,3 +79,48 @@ def test_noalloc_rejects_batch_beyond_fixed_scratch():
     assert rc == -4  # PKV_ERR_WORKSPACE, nothing launched
     torch.cuda.synchronize()
     assert bool((out == 7.0).all())
+
+
+def _largest_batch_fitting(hq: int) -> int:
+    """Largest batch whose decode scratch fits the fixed array on this GPU,
+    from the library's own size query (so no SM count is assumed)."""
+    lo, hi = 0, 1
+    while pkv.decode_workspace_bytes(hi, hq) <= STATIC_SCRATCH_BYTES:
+        lo, hi = hi, hi * 2
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if pkv.decode_workspace_bytes(mid, hq) <= STATIC_SCRATCH_BYTES:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def test_noalloc_batch_limit_exact():
+    """At the largest batch whose scratch fits, the call runs and matches
+    pkv_paged_attn_decode; one sequence more is refused before any launch."""
+    hq = 16
+    bmax = _largest_batch_fitting(hq)
+    assert pkv.decode_workspace_bytes(bmax, hq) <= STATIC_SCRATCH_BYTES < pkv.decode_workspace_bytes(bmax + 1, hq)
+    fn = _noalloc_fn()
+    rng = np.random.default_rng(855)
+    lens = rng.integers(1, 700, size=bmax)
+    w = W.make_decode("limit", 855, lens, hq, 8)
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.kv_cache_write(to_dev(w.k_new), to_dev(w.v_new), i32(w.slot_mapping), kc, vc)
+    q, ctx, tab = to_dev(w.q), i32(w.context_lens), i32(w.block_tables)
+    ref = to_host(pkv.paged_attn_decode(q, kc, vc, ctx, tab, w.scale, max_context_len=w.max_context_len))
+    out = torch.full_like(q, float("nan"))
+    rc = _call_noalloc(fn, q, kc, vc, ctx, tab, w, out)
+    assert rc == 0, pkv.STATUS.get(rc, rc)
+    torch.cuda.synchronize()
+    check_close(to_host(out), W.bf16_bits_to_f32(ref).astype(np.float64), "noalloc at the batch limit")
+    # One more sequence (a pad row) no longer fits: refused, nothing launched.
+    w2 = W.make_decode("limit_plus_one", 856, lens, hq, 8, pad_to=bmax + 1, fill_caches=False)
+    q2 = torch.zeros((bmax + 1, hq, 128), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.full_like(q2, 7.0)
+    rc = _call_noalloc(fn, q2, kc, vc, i32(w2.context_lens), i32(w2.block_tables), w2, out2)
+    assert rc == -4  # PKV_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((out2 == 7.0).all())
+    assert pkv.device_error() == []
