@@ -386,21 +386,30 @@ def run_pkv(args, rank, world, local):
     dec_ms = ms / LAYERS
     clk = clocks.summary()
 
-    # end to end: every step's inputs (each layer's q, k_new, v_new and the
-    # step metadata) come from pinned host memory and every layer's output
-    # goes back to pinned host memory, through the public call.  A copy stream
-    # brings step s+1's inputs in while step s computes and drains step s-1's
-    # outputs (double-buffered on the device), so inside a step the 28 calls
-    # run back to back with programmatic dependent launch intact.
+    # end to end, through the device-chained step graph (DecodeStepGraph): per
+    # step the host sends each layer's q, k_new, v_new and, for the step
+    # metadata, only what each sequence holds -- its block list (a CSR pair),
+    # num_cached and length -- from pinned memory; the replayed graph derives
+    # the slots, context lengths and packed tables on the device and runs the
+    # 28 fused write + decode calls; every layer's output comes back to pinned
+    # host memory.  Two buffer sets: a copy stream stages step s+1 while step
+    # s replays and drains step s-1's outputs.
+    from paged_kv_cache_304_gb300.graphs import DecodeStepGraph
+
+    L_host = w.context_lens.astype(np.int64)
+    lists = [w.block_tables[i, :-(-int(L_host[i]) // 256)] for i in range(B)]
+    offs = np.zeros(B + 1, np.int32)
+    offs[1:] = np.cumsum([x.size for x in lists])
     h_q = qs.cpu().pin_memory()
     h_k = ks.cpu().pin_memory()
     h_v = vs.cpu().pin_memory()
-    h_meta = [torch.from_numpy(a).pin_memory() for a in (w.slot_mapping, w.context_lens, w.block_tables)]
-    h_out = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
-    d_in = [[torch.empty_like(t, device=device) for t in (h_q, h_k, h_v, *h_meta)] for _ in range(2)]
-    d_out = [torch.empty_like(outs) for _ in range(2)]
-    copy = torch.cuda.Stream(device)
+    h_meta = [torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).pin_memory()
+              for a in (np.concatenate(lists), offs, L_host - 1, L_host)]
     h_src = (h_q, h_k, h_v, *h_meta)
+    h_out = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
+    step_graph = DecodeStepGraph([(kv[0, l], kv[1, l]) for l in range(LAYERS)], hq, w.max_blocks_per_seq, w.scale,
+                                 w.num_blocks, max_batch=B, max_context_len=maxctx, buckets=[B], buffer_sets=2)
+    copy = torch.cuda.Stream(device)
 
     def run_e2e(nsteps):
         ev = lambda: [torch.cuda.Event() for _ in range(nsteps)]
@@ -409,9 +418,9 @@ def run_pkv(args, rank, world, local):
         def load(s):
             with torch.cuda.stream(copy):
                 if s >= 2:
-                    copy.wait_event(in_free[s - 2])  # step s-2 has finished reading this buffer
-                for dst, src in zip(d_in[s % 2], h_src):
-                    dst.copy_(src, non_blocking=True)
+                    copy.wait_event(in_free[s - 2])   # step s-2 has finished reading this set
+                    copy.wait_event(out_free[s - 2])  # and its outputs have left it
+                step_graph.stage(*h_src, buffer_set=s % 2)
                 in_ready[s].record(copy)
 
         copy.wait_stream(stream)
@@ -419,19 +428,13 @@ def run_pkv(args, rank, world, local):
         for s in range(nsteps):
             if s + 1 < nsteps:
                 load(s + 1)
-            dq, dk, dv, dslots, dctx, dtab = d_in[s % 2]
             stream.wait_event(in_ready[s])
-            if s >= 2:
-                stream.wait_event(out_free[s - 2])  # step s-2's outputs have left this buffer
-            for l in range(LAYERS):
-                pkv.paged_attn_decode_fused_write(dq[l], dk[l], dv[l], dslots, kv[0, l], kv[1, l], dctx, dtab,
-                                                  w.scale, out=d_out[s % 2][l], workspace=ws,
-                                                  max_context_len=maxctx)
+            out = step_graph.replay(B, buffer_set=s % 2)
             in_free[s].record(stream)
             done[s].record(stream)
             with torch.cuda.stream(copy):
                 copy.wait_event(done[s])
-                h_out.copy_(d_out[s % 2], non_blocking=True)
+                h_out.copy_(out, non_blocking=True)
                 out_free[s].record(copy)
         stream.wait_stream(copy)
 
@@ -447,6 +450,8 @@ def run_pkv(args, rank, world, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
     h2d = sum(t.numel() * t.element_size() for t in h_src)
     d2h = h_out.numel() * h_out.element_size()
+    e2e_out_ok = bool(torch.equal(h_out.to(device), outs))  # the chained step gives the eager step's outputs
+    del step_graph
 
     # the same step with the write fused into decode, and both captured once
     # as a CUDA graph (bucket = batch) and replayed
@@ -524,7 +529,10 @@ def run_pkv(args, rank, world, local):
                      "traffic": recorded_traffic() if LAYERS == 28 or LAYERS == 1 else None},
         "clocks": clk,
         "e2e": {"value": round(step_bytes * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "DecodeStepGraph: per-sequence block lists and lengths in, metadata on the device, "
+                        "28 fused write+decode calls replayed from one graph",
+                "outputs_equal_eager_step": e2e_out_ok},
         "gpu_launches": args.steps * LAYERS * 2,
         "extra": extra,
     }

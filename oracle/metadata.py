@@ -13,11 +13,17 @@ legs use it.  What it computes follows nano-vllm as described on the page
 * the varlen attention calls take cumulative sequence lengths of the new
   tokens (queries) and of all tokens (keys) ("第六站：注意力层").
 
+* a CUDA-graph step is padded to its captured batch size with rows whose
+  slot is -1 and whose context length is 0 ("第五站", CUDA Graph paragraph);
+  here such a pad row is a sequence with c_i = L_i = 0: it adds no new
+  tokens and no keys, its context length is 0 and its table row is -1.
+
 Inputs per sequence i: its block table (list of physical block ids),
 num_cached c_i and length L_i (tokens in the cache after this step,
-c_i < L_i).  Outputs: cu_seqlens_q, cu_seqlens_k ([S+1]), context_lens
-(= L), slot_mapping (one entry per new token, sequence by sequence) and the
-block tables packed to [S, max_blocks] with -1 padding.
+c_i < L_i, or c_i = L_i = 0 for a pad row).  Outputs: cu_seqlens_q,
+cu_seqlens_k ([S+1]), context_lens (= L), slot_mapping (one entry per new
+token, sequence by sequence) and the block tables packed to [S, max_blocks]
+with -1 padding.
 """
 
 from __future__ import annotations
@@ -31,7 +37,8 @@ def prepare_metadata(tables, num_cached, seq_lens, max_blocks: int, block_size: 
     packed = [[-1] * max_blocks for _ in range(S)]
     for i in range(S):
         c, L, tab = int(num_cached[i]), int(seq_lens[i]), list(tables[i])
-        if not (0 <= c < L) or len(tab) * block_size < L or len(tab) > max_blocks:
+        pad = c == 0 and L == 0
+        if (not pad and not (0 <= c < L)) or len(tab) * block_size < L or len(tab) > max_blocks:
             raise ValueError(f"sequence {i}: need 0 <= cached < length <= blocks * block_size")
         cu_q[i + 1] = cu_q[i] + (L - c)
         cu_k[i + 1] = cu_k[i] + L

@@ -266,13 +266,15 @@ def paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
 
 def prepare_metadata(block_ids: torch.Tensor, table_offsets: torch.Tensor, num_cached: torch.Tensor,
                      seq_lens: torch.Tensor, token_capacity: int, max_blocks_per_seq: int, num_blocks: int,
-                     block_size: int = 256) -> dict:
+                     block_size: int = 256, out: dict | None = None) -> dict:
     """Step metadata on the device from per-sequence (block table, num_cached, length).
 
     block_ids/table_offsets: the block tables as a CSR pair (int32); num_cached,
-    seq_lens: [S] int32.  Returns device tensors cu_seqlens_q, cu_seqlens_k,
-    context_lens, slot_mapping [token_capacity] (-1 past the real tokens) and
-    block_tables [S, max_blocks_per_seq].
+    seq_lens: [S] int32 (num_cached = seq_len = 0 marks a CUDA-graph pad row).
+    Returns device tensors cu_seqlens_q, cu_seqlens_k, context_lens,
+    slot_mapping [token_capacity] (-1 past the real tokens) and block_tables
+    [S, max_blocks_per_seq]; `out` may hold preallocated tensors of those
+    names and shapes (int32, contiguous) to write into instead.
     """
     lib = load()
     for t, n in ((block_ids, "block_ids"), (table_offsets, "table_offsets"), (num_cached, "num_cached"),
@@ -284,13 +286,16 @@ def prepare_metadata(block_ids: torch.Tensor, table_offsets: torch.Tensor, num_c
     if num_cached.shape != (S,) or table_offsets.shape != (S + 1,):
         raise ValueError("num_cached must be [S] and table_offsets [S+1]")
     dev = seq_lens.device
-    out = {
-        "cu_seqlens_q": torch.empty(S + 1, dtype=torch.int32, device=dev),
-        "cu_seqlens_k": torch.empty(S + 1, dtype=torch.int32, device=dev),
-        "context_lens": torch.empty(S, dtype=torch.int32, device=dev),
-        "slot_mapping": torch.empty(max(token_capacity, 0), dtype=torch.int32, device=dev),
-        "block_tables": torch.empty((S, max_blocks_per_seq), dtype=torch.int32, device=dev),
-    }
+    shapes = {"cu_seqlens_q": (S + 1,), "cu_seqlens_k": (S + 1,), "context_lens": (S,),
+              "slot_mapping": (max(token_capacity, 0),), "block_tables": (S, max_blocks_per_seq)}
+    if out is None:
+        out = {k: torch.empty(v, dtype=torch.int32, device=dev) for k, v in shapes.items()}
+    else:
+        for k, v in shapes.items():
+            t = out[k]
+            _dev(t, k, torch.int32)
+            if tuple(t.shape) != v or not t.is_contiguous():
+                raise ValueError(f"out[{k!r}] must be a contiguous int32 tensor of shape {v}")
     _check("pkv_prepare_metadata", lib.pkv_prepare_metadata(
         block_ids.data_ptr(), table_offsets.data_ptr(), num_cached.data_ptr(), seq_lens.data_ptr(), S,
         int(token_capacity), int(max_blocks_per_seq), int(block_size), int(num_blocks),

@@ -16,7 +16,9 @@
 //   inclusive scans give cu_seqlens_q and cu_seqlens_k; context_lens = L.
 //   A sequence whose table is too short for L_i (the decode rule: a token at
 //   position L-1 with L % block_size == 1 needs a fresh block) or whose
-//   lengths are inconsistent is flagged and contributes no tokens.
+//   lengths are inconsistent is flagged and contributes no tokens; one with
+//   no tokens at all (num_cached = L = 0) is a CUDA-graph pad row and
+//   contributes none without a flag.
 // * fill (grid): thread t < token capacity finds its sequence by binary search
 //   in cu_seqlens_q and writes its slot (or -1 past the last real token, the
 //   CUDA-graph padding value); thread e < S * max_blocks writes one entry of
@@ -46,11 +48,17 @@ struct MetaParams {
   int32_t* tables;      // [S, max_blocks]
 };
 
-// n_i and L_i of sequence i, or (0, 0) (flagged) if its inputs are inconsistent.
+// n_i and L_i of sequence i, or (0, 0) (flagged) if its inputs are
+// inconsistent.  A sequence with num_cached == seq_len == 0 is a CUDA-graph
+// pad row: it contributes no tokens and context length 0, unflagged.
 __device__ __forceinline__ void seq_counts(const MetaParams& p, int i, int& n, int& L) {
   const int c = __ldg(p.num_cached + i);
   L = __ldg(p.seq_lens + i);
   const int nb = __ldg(p.table_offsets + i + 1) - __ldg(p.table_offsets + i);
+  if (c == 0 && L == 0 && nb >= 0 && nb <= p.max_blocks) {
+    n = 0;
+    return;
+  }
   if (c < 0 || L <= c || nb < 0 || nb > p.max_blocks || static_cast<int64_t>(nb) * p.block_size < L) {
     atomicOr(&g_err_metadata, PKV_DEVERR_LEN_RANGE);
     n = 0;

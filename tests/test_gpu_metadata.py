@@ -86,3 +86,21 @@ def test_short_table_is_flagged_and_skipped():
     got, _ = _run([[3], [5, 6]], [255, 0], [257, 300], 2, 8, capacity=300)
     assert "LEN_RANGE" in pkv.device_error()
     assert got["cu_seqlens_q"].tolist() == [0, 0, 300]  # sequence 0 contributes nothing
+
+
+def test_graph_pad_rows_unflagged():
+    """Pad rows (num_cached = length = 0, empty table) after the real rows of
+    the padded decode workload: no flag, context length 0, -1 tables, and the
+    real rows' slots followed by -1."""
+    w = W.graph_padded_decode(fill_caches=False)
+    L = w.context_lens.astype(np.int64)
+    real = w.real_batch
+    tables = _tables_of(w, L[:real]) + [[]] * (w.batch - real)
+    cached = np.concatenate([L[:real] - 1, np.zeros(w.batch - real, np.int64)])
+    pkv.device_error(clear=True)
+    got, total = _run(tables, cached, L, w.max_blocks_per_seq, w.num_blocks, capacity=w.batch)
+    assert total == real
+    assert pkv.device_error() == []
+    assert np.array_equal(got["slot_mapping"], w.slot_mapping)
+    assert np.array_equal(got["context_lens"], w.context_lens)
+    assert np.array_equal(got["block_tables"], w.block_tables)

@@ -53,3 +53,28 @@ def test_prefill_workloads_agree_with_generator(name):
 def test_rejects_short_table():
     with pytest.raises(ValueError):
         prepare_metadata([[3]], [255], [257], max_blocks=2)  # position 256 needs a second block
+
+
+def test_graph_pad_rows_reproduce_the_padded_decode_workload():
+    """The CUDA-graph padded decode step (500 real rows padded to 512 with
+    slot -1 and context length 0, built by the input generator): pad rows
+    given as empty sequences (num_cached = length = 0, no table) add no
+    tokens, get context length 0 and a -1 table row, so the real rows' slots
+    followed by -1 up to the padded batch are exactly the generator's slot
+    mapping."""
+    w = W.graph_padded_decode(fill_caches=False)
+    L = w.context_lens.astype(np.int64)
+    real = w.real_batch
+    tables = [list(w.block_tables[i, :-(-int(L[i]) // 256)]) for i in range(real)] + [[]] * (w.batch - real)
+    cached = np.concatenate([L[:real] - 1, np.zeros(w.batch - real, np.int64)])
+    m = prepare_metadata(tables, cached, L, max_blocks=w.max_blocks_per_seq)
+    slots = m["slot_mapping"] + [-1] * (w.batch - len(m["slot_mapping"]))
+    assert slots == w.slot_mapping.tolist()
+    assert m["context_lens"] == w.context_lens.tolist()
+    assert np.array_equal(np.array(m["block_tables"]), w.block_tables)
+    assert m["cu_seqlens_q"][real:] == [real] * (w.batch - real + 1)
+
+
+def test_rejects_empty_sequence_with_cached_tokens():
+    with pytest.raises(ValueError):
+        prepare_metadata([[3]], [5], [5], max_blocks=2)  # no new token but not a pad row
