@@ -673,7 +673,7 @@ def _write_extra(torch, pkv, device, gen, w, pk, reps=20):
             "bytes": nbytes, "l2": "evicted between reps (256 MB read)"}
 
 
-def _prefill_extra(torch, pkv, device, gen, w: W.PrefillWorkload, pk, reps=10):
+def _prefill_extra(torch, pkv, device, gen, w: W.PrefillWorkload, pk, reps=10, step_too=False):
     kv = make_cache(torch, 1, w.num_blocks, w.num_kv_heads, gen, device)
     q = torch.randn(w.q.shape, generator=gen, device=device).to(torch.bfloat16)
     cq = torch.from_numpy(w.cu_seqlens_q).to(device)
@@ -687,9 +687,29 @@ def _prefill_extra(torch, pkv, device, gen, w: W.PrefillWorkload, pk, reps=10):
         return {"unavailable": str(e)}
     flops = prefill_flops(w)
     tf = flops / (ms / 1e3) / 1e12
+    res = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_of_measured_bf16": round(tf / pk["bf16_tflops"], 4),
+           "flops": flops}
+    if step_too:
+        # the whole prefill step of one layer: the KV write of the new tokens
+        # then attention, as two calls and as the one fused call
+        kn = torch.randn(w.k_new.shape, generator=gen, device=device).to(torch.bfloat16)
+        vn = torch.randn(w.v_new.shape, generator=gen, device=device).to(torch.bfloat16)
+        slots = torch.from_numpy(w.slot_mapping).to(device)
+        ws = pkv.prefill_fused_workspace(device)
+
+        def separate():
+            pkv.kv_cache_write(kn, vn, slots, kv[0, 0], kv[1, 0])
+            pkv.paged_attn_prefill(q, kv[0, 0], kv[1, 0], cq, ck, tab, w.scale, w.max_seqlen_q, w.max_seqlen_k,
+                                   out=out)
+
+        def fused():
+            pkv.paged_attn_prefill_fused_write(q, kn, vn, slots, kv[0, 0], kv[1, 0], cq, ck, tab, w.scale,
+                                               w.max_seqlen_q, w.max_seqlen_k, out=out, workspace=ws)
+
+        res["step_write_then_prefill_ms"] = round(_time_calls(torch, separate, reps), 4)
+        res["step_fused_write_prefill_ms"] = round(_time_calls(torch, fused, reps), 4)
     del kv
-    return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_of_measured_bf16": round(tf / pk["bf16_tflops"], 4),
-            "flops": flops}
+    return res
 
 
 def _metadata_extra(torch, pkv, device, w, reps=20):
@@ -739,9 +759,10 @@ def run_extras(torch, pkv, device, gen, pk):
     out["kv_write_qwen3_8b_prefill_32768_tokens"] = _write_extra(torch, pkv, device, gen,
                                                                  W.qwen3_8b_prefill(fill_caches=False), pk)
     out["chunked_prefill_prefix_budget16384"] = _prefill_extra(torch, pkv, device, gen,
-                                                               W.chunked_prefill_prefix(fill_caches=False), pk)
+                                                               W.chunked_prefill_prefix(fill_caches=False), pk,
+                                                               step_too=True)
     out["qwen3_8b_prefill_4x8192"] = _prefill_extra(torch, pkv, device, gen, W.qwen3_8b_prefill(fill_caches=False),
-                                                    pk)
+                                                    pk, step_too=True)
     torch.cuda.empty_cache()
     return out
 
@@ -767,10 +788,10 @@ def run_case(args, local):
         else:  # a smaller pool for profiling runs
             w = W.make_prefill(f"qwen3_8b_prefill_{n}x8192", 3045, [8192] * n, [0] * n, 32, 8,
                                num_blocks=32 * n + 8, fill_caches=False)
-        res = _prefill_extra(torch, pkv, device, gen, w, pk, reps=reps)
+        res = _prefill_extra(torch, pkv, device, gen, w, pk, reps=reps, step_too=True)
     elif args.case == "prefill_chunked":
         w = W.chunked_prefill_prefix(fill_caches=False)
-        res = _prefill_extra(torch, pkv, device, gen, w, pk, reps=reps)
+        res = _prefill_extra(torch, pkv, device, gen, w, pk, reps=reps, step_too=True)
     elif args.case == "decode_8b":
         w = W.qwen3_8b_decode(fill_caches=False)
         res = _decode_extra(torch, pkv, device, gen, w, pk, reps=reps)

@@ -220,6 +220,43 @@ PKV_API pkv_status pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_c
                            pkv_bf16* out, void* stream);
 
 /*
+ * Prefill attention with the KV-cache write fused in: the same result as
+ * pkv_kv_cache_write(k_new, v_new, slot_mapping, ...) of the step's total_q
+ * new tokens followed by pkv_paged_attn_prefill(...), in one call (page
+ * section "第六站：注意力层": in prefill and decode alike the step's K/V are
+ * written into the cache first, then attention reads the cache).  Every SM
+ * writes a share of the new rows, then waits at a grid-wide barrier for all
+ * others before the first cache read, so the write costs no launch of its own
+ * and its rows are still in L2 when attention reads them.
+ *
+ *   k_new, v_new   [total_q, num_kv_heads, head_dim] bf16, token i's row at
+ *                  element i * k_token_stride (resp. v_token_stride);
+ *                  16-byte aligned, strides multiples of 8 elements.
+ *   slot_mapping   [total_q] int32: the cache slot of new token i, or -1
+ *                  (skipped).  Out-of-range slots are skipped and flag
+ *                  PKV_DEVERR_SLOT_RANGE.
+ *   k_cache, v_cache  written at those slots, then read as in
+ *                  pkv_paged_attn_prefill.
+ *   workspace      >= pkv_prefill_fused_workspace_bytes() bytes, 16-byte
+ *                  aligned, ZEROED before its first use (e.g. by cudaMemset
+ *                  when allocated); every call leaves it ready for the next.
+ *                  Two calls that may run concurrently need two workspaces.
+ *                  If a call reports PKV_DEVERR_WAIT_TIMEOUT, zero it again.
+ * Every other argument is as in pkv_paged_attn_prefill.  The call always uses
+ * the persistent kernel (one CTA per SM, launched cooperatively so that all of
+ * them are resident at the barrier); a launch that cannot be co-resident
+ * returns PKV_ERR_CUDA.
+ */
+PKV_API size_t pkv_prefill_fused_workspace_bytes(void);
+PKV_API pkv_status pkv_paged_attn_prefill_fused_write(
+    const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride, const pkv_bf16* v_new,
+    int64_t v_token_stride, const int32_t* slot_mapping, pkv_bf16* k_cache, pkv_bf16* v_cache,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+    int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float scale, pkv_bf16* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Decode attention without caller scratch: the same computation and
  * arguments as pkv_paged_attn_decode, minus `workspace`/`workspace_bytes`.
  * The pages have no counterpart to this call; it exists for callers that

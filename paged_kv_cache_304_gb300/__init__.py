@@ -90,6 +90,11 @@ def load(path: str | None = None):
         lib.pkv_sample_exponential_race.argtypes = [vp, i64, vp, i32, i32, ctypes.c_uint64, ctypes.c_uint64, vp, vp,
                                                     sz, vp]
         lib.pkv_sample_exponential_race.restype = ctypes.c_int
+        lib.pkv_prefill_fused_workspace_bytes.argtypes = []
+        lib.pkv_prefill_fused_workspace_bytes.restype = sz
+        lib.pkv_paged_attn_prefill_fused_write.argtypes = [vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                           i32, i32, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]
+        lib.pkv_paged_attn_prefill_fused_write.restype = ctypes.c_int
         lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         lib.pkv_device_error.restype = ctypes.c_int
         if path is None:
@@ -261,6 +266,59 @@ def paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
         block_tables.data_ptr(), int(block_tables.shape[1]), S, T, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
         bs, nb, float(scale), out.data_ptr(), _stream(q)))
+    return out
+
+
+def prefill_fused_workspace(device) -> torch.Tensor:
+    """A zeroed workspace for paged_attn_prefill_fused_write (reusable by the
+    calls of one stream)."""
+    n = int(load().pkv_prefill_fused_workspace_bytes())
+    return torch.zeros(max(256, n), dtype=torch.uint8, device=device)
+
+
+def paged_attn_prefill_fused_write(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                   slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                                   block_tables: torch.Tensor, scale: float, max_seqlen_q: int, max_seqlen_k: int,
+                                   out: torch.Tensor | None = None,
+                                   workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """kv_cache_write of the step's new tokens then paged_attn_prefill, in one call.
+
+    k_new, v_new [T, Hkv, D] bf16 with rows 16-byte aligned; slot_mapping [T]
+    int32; workspace: from prefill_fused_workspace() (zeroed once, then reused).
+    """
+    lib = load()
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev(t, n, torch.bfloat16)
+    for t, n in ((slot_mapping, "slot_mapping"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k"),
+                 (block_tables, "block_tables")):
+        _dev(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    T, hq, dq = (int(x) for x in q.shape)
+    if dq != d or not q.is_contiguous():
+        raise ValueError("q must be contiguous [T, Hq, head_dim]")
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if t.dim() != 3 or tuple(t.shape) != (T, hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{n} must be [T, Hkv, head_dim] with contiguous rows")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [T]")
+    S = int(cu_seqlens_q.shape[0]) - 1
+    if cu_seqlens_k.shape[0] != S + 1 or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("cu_seqlens_k must be [S+1] and block_tables [S, max_blocks]")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if workspace is None:
+        workspace = prefill_fused_workspace(q.device)
+    _check("pkv_paged_attn_prefill_fused_write", lib.pkv_paged_attn_prefill_fused_write(
+        q.data_ptr(), k_new.data_ptr(), k_new.stride(0), v_new.data_ptr(), v_new.stride(0), slot_mapping.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+        block_tables.data_ptr(), int(block_tables.shape[1]), S, T, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d,
+        bs, nb, float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(q)))
     return out
 
 

@@ -17,6 +17,7 @@ namespace {
 
 constexpr int kDecodeTileTokens = 16;    // must match kT in decode.cu
 constexpr int kPrefillTileTokens = 128;  // must match kTileN in prefill.cu
+constexpr size_t kPrefillFusedWorkspaceBytes = 256;  // grid-barrier words of the fused-write prefill
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -188,6 +189,68 @@ pkv_status decode_common(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_b
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Shared by the plain and the fused-write prefill entry points.
+pkv_status prefill_common(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                           int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale, pkv_bf16* out, void* stream, PrefillArgs& a) {
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PKV_ERR_SHAPE;
+  const pkv_status st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
+  if (st != PKV_OK) return st;
+  if (max_seqlen_q > max_seqlen_k) return PKV_ERR_SHAPE;
+  if (num_seqs > 65535 || max_seqlen_q > (1 << 22) || max_seqlen_k >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
+  if (total_q == 0 || num_seqs == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+  auto enc = encode_fn();
+  if (!enc) return PKV_ERR_CUDA;
+  CUtensorMap qmap;
+  {
+    // q [total_q, Hq, 128]: boxes of 128 rows x 64 dims of one head, swizzled.
+    cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
+    cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(num_q_heads) * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<pkv_bf16*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  }
+  CUtensorMap omap;
+  {
+    // out, same layout as q: boxes of 32 rows (one warp's rows) x 64 dims of
+    // one head, swizzled, for the bulk tensor stores of the epilogue.
+    cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
+    cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(num_q_heads) * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, 32};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  }
+  CacheMaps maps;
+  if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kPrefillTileTokens, 1, &maps))
+    return PKV_ERR_CUDA;
+  a.q = q;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.block_tables = block_tables;
+  a.out = out;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  cudaError_t e = launch_paged_attn_prefill(a, maps, qmap, omap, sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -230,65 +293,46 @@ pkv_status pkv_paged_attn_decode_fused_write(const pkv_bf16* q, const pkv_bf16* 
 }
 
 pkv_status pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
-                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_tables,
-                           int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
-                           int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                           int32_t block_size, int32_t num_blocks, float scale, pkv_bf16* out, void* stream) {
-  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return PKV_ERR_SHAPE;
-  const pkv_status st = check_attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale);
-  if (st != PKV_OK) return st;
-  if (max_seqlen_q > max_seqlen_k) return PKV_ERR_SHAPE;
-  if (num_seqs > 65535 || max_seqlen_q > (1 << 22) || max_seqlen_k >= (1 << 26)) return PKV_ERR_UNSUPPORTED;
-  if (total_q == 0 || num_seqs == 0 || max_seqlen_q == 0) return PKV_OK;
-  if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables || !out) return PKV_ERR_NULL;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
-  auto enc = encode_fn();
-  if (!enc) return PKV_ERR_CUDA;
-  CUtensorMap qmap;
-  {
-    // q [total_q, Hq, 128]: boxes of 128 rows x 64 dims of one head, swizzled.
-    cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
-    cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(num_q_heads) * kHeadDim * 2};
-    cuuint32_t box[3] = {64, 1, 128};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<pkv_bf16*>(q), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return PKV_ERR_CUDA;
-  }
-  CUtensorMap omap;
-  {
-    // out, same layout as q: boxes of 32 rows (one warp's rows) x 64 dims of
-    // one head, swizzled, for the bulk tensor stores of the epilogue.
-    cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
-    cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(num_q_heads) * kHeadDim * 2};
-    cuuint32_t box[3] = {64, 1, 32};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return PKV_ERR_CUDA;
-  }
-  CacheMaps maps;
-  if (!encode_cache_maps(k_cache, v_cache, num_blocks, num_kv_heads, kPrefillTileTokens, 1, &maps))
-    return PKV_ERR_CUDA;
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                                  int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  float scale, pkv_bf16* out, void* stream) {
   PrefillArgs a;
-  a.q = q;
-  a.cu_seqlens_q = cu_seqlens_q;
-  a.cu_seqlens_k = cu_seqlens_k;
-  a.block_tables = block_tables;
-  a.out = out;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_seqs = num_seqs;
-  a.total_q = total_q;
-  a.max_seqlen_q = max_seqlen_q;
-  a.max_seqlen_k = max_seqlen_k;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.num_blocks = num_blocks;
-  a.scale = scale;
-  cudaError_t e = launch_paged_attn_prefill(a, maps, qmap, omap, sm_count(), static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return prefill_common(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_blocks_per_seq, num_seqs,
+                        total_q, max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, scale, out, stream, a);
+}
+
+size_t pkv_prefill_fused_workspace_bytes(void) { return kPrefillFusedWorkspaceBytes; }
+
+pkv_status pkv_paged_attn_prefill_fused_write(
+    const pkv_bf16* q, const pkv_bf16* k_new, int64_t k_token_stride, const pkv_bf16* v_new, int64_t v_token_stride,
+    const int32_t* slot_mapping, pkv_bf16* k_cache, pkv_bf16* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+    int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, pkv_bf16* out, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (total_q > 0 && num_seqs > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_NULL;
+    if (k_token_stride < row || v_token_stride < row) return PKV_ERR_SHAPE;
+    if (k_token_stride % 8 || v_token_stride % 8 || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGN;
+    if (!workspace || workspace_bytes < kPrefillFusedWorkspaceBytes) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return PKV_ERR_ALIGN;
+  }
+  PrefillArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_stride = k_token_stride;
+  a.v_stride = v_token_stride;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.barrier_ws = static_cast<unsigned int*>(workspace);
+  return prefill_common(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_blocks_per_seq, num_seqs,
+                        total_q, max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, scale, out, stream, a);
 }
 
 // ---------------------------------------------------------------------------

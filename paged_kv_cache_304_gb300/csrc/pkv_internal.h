@@ -120,6 +120,18 @@ struct PrefillArgs {
   int32_t num_kv_heads;
   int32_t num_blocks;
   float scale;
+  // Fused KV write (optional; all null for plain prefill): token i's new row
+  // k_new[i] / v_new[i] (token strides in elements) goes to k_cache / v_cache
+  // at slot_mapping[i] before any cache read; barrier_ws is the caller's
+  // two-word grid-barrier workspace.
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
+  int64_t k_stride = 0;
+  int64_t v_stride = 0;
+  const int32_t* slot_mapping = nullptr;
+  uint16_t* k_cache = nullptr;
+  uint16_t* v_cache = nullptr;
+  unsigned int* barrier_ws = nullptr;
 };
 // Stated max_seqlen_q up to which the persistent kernel is used (prefill.cu
 // dispatches; prefill_persistent.cu holds that kernel).

@@ -574,7 +574,9 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
   if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
   // Short query tiles: a CTA launch per 128-row tile costs about as much as
   // the tile's tensor work, so they go to the persistent kernel.
-  if (a.max_seqlen_q <= kPersistentMaxSeqlenQ) return launch_prefill_persistent(a, kv, qmap, omap, num_sms, stream);
+  // The fused KV write needs every CTA resident at once (a grid barrier
+  // separates the write from the first cache read): also the persistent kernel.
+  if (a.max_seqlen_q <= kPersistentMaxSeqlenQ || a.k_new) return launch_prefill_persistent(a, kv, qmap, omap, num_sms, stream);
   PrefillParams p;
   p.cu_q = a.cu_seqlens_q;
   p.cu_k = a.cu_seqlens_k;

@@ -85,6 +85,20 @@ constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 1);  // B = V
 constexpr uint64_t kDrainNs = 100000000ull;  // bound of the waits that drain in-flight work
 constexpr uint32_t kSleepNs = 200;  // polling interval of the waits off the critical path
 
+// The KV write fused in front of the attention (optional): every new token's
+// K and V row goes to its cache slot before any CTA reads the cache.
+struct FusedWrite {
+  const uint16_t* k_new;  // null: no fused write
+  const uint16_t* v_new;
+  int64_t k_stride, v_stride;  // elements between token rows
+  const int32_t* slots;        // [num_tokens]
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  int64_t num_slots;
+  int32_t num_tokens, row_elems;  // row_elems = num_kv_heads * 128
+  unsigned int* barrier;          // caller workspace: [0] arrivals, [1] epoch
+};
+
 struct PrefillParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
@@ -92,6 +106,7 @@ struct PrefillParams {
   uint16_t* out;
   int32_t maxb, S, Hq, Hkv, G, npairs, num_blocks, total_q, per_half, max_tiles;
   float sl2;  // scale * log2(e)
+  FusedWrite fw;
 };
 
 // One work item: a 128-row query tile of one sequence for one head pair.
@@ -941,6 +956,70 @@ __device__ void run_epilogue(const PrefillParams& p, const Smem& sm, const CUten
   __syncwarp();
 }
 
+// ------------------------------------------------------------ fused KV write
+// One warp per token row (like the standalone write kernel): 16-byte loads
+// of the new K and V rows, 16-byte stores into the cache slot; slot -1 is
+// skipped, an out-of-range slot flagged and skipped.  The stores are then
+// made visible to the bulk-copy (async) proxy that the attention's loads use.
+__device__ void write_new_rows(const PrefillParams& p) {
+  const int warps = kThreads / 32;
+  const int lane = threadIdx.x & 31;
+  const int nvec = p.fw.row_elems / 8;  // 16-byte vectors per row
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < p.fw.num_tokens; t += gridDim.x * warps) {
+    const int slot = __ldg(p.fw.slots + t);
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= p.fw.num_slots) {
+      if (lane == 0) atomicOr(&g_err_prefill_persistent, PKV_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const uint4* ks = reinterpret_cast<const uint4*>(p.fw.k_new + static_cast<int64_t>(t) * p.fw.k_stride);
+    const uint4* vs = reinterpret_cast<const uint4*>(p.fw.v_new + static_cast<int64_t>(t) * p.fw.v_stride);
+    uint4* kd = reinterpret_cast<uint4*>(p.fw.k_cache + static_cast<int64_t>(slot) * p.fw.row_elems);
+    uint4* vd = reinterpret_cast<uint4*>(p.fw.v_cache + static_cast<int64_t>(slot) * p.fw.row_elems);
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 kv = __ldg(ks + i), vv = __ldg(vs + i);
+      kd[i] = kv;
+      vd[i] = vv;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Grid-wide barrier on the caller's two-word workspace (arrival count, epoch;
+// both zero before the first call).  The last CTA to arrive resets the count
+// and advances the epoch; the others wait (bounded, two seconds) for the
+// epoch to move.  The launch is cooperative, so every CTA is resident.
+// Returns false (flagging PKV_DEVERR_WAIT_TIMEOUT) if the wait gave up.
+__device__ bool grid_barrier(unsigned int* bar, int* ok_smem) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int* vb = bar;
+    const unsigned int e = vb[1];
+    __threadfence();
+    bool ok = true;
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (vb[1] == e) {
+        __nanosleep(64);
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+          atomicOr(&g_err_prefill_persistent, PKV_DEVERR_WAIT_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    *ok_smem = ok;
+  }
+  __syncthreads();
+  return *reinterpret_cast<volatile int*>(ok_smem) != 0;
+}
+
 __device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl)); }
 __device__ __forceinline__ void regs_dec_epi() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsEpi)); }
 __device__ __forceinline__ void regs_inc_softmax() {
@@ -1003,9 +1082,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.gen + kOffTmem);
   // columns: S 0-127, P_A 128-191, P_B 192-255, O_A 256-383, O_B 384-511
 
+  // With the write fused in: every CTA writes its share of the new rows,
+  // then all wait for each other before the first cache read.
+  bool run = true;
+  if (p.fw.k_new) {
+    write_new_rows(p);
+    run = grid_barrier(p.fw.barrier, sm.abort());
+    if (threadIdx.x == 0) *sm.abort() = 0;
+    __syncthreads();
+  }
+
   // Warpgroup 0 (producer, MMA issuers, scheduler) and 3 (epilogue) give
   // registers to warpgroups 1 and 2 (softmax).
-  if (warp < kWarpSoftmax) {
+  if (!run) {
+    // the barrier gave up: no attention (flagged)
+  } else if (warp < kWarpSoftmax) {
     regs_dec_ctl();
     if (warp == kWarpSched) {
       run_scheduler(p, sm, lane);
@@ -1048,6 +1139,20 @@ cudaError_t launch_prefill_persistent(const PrefillArgs& a, const CacheMaps& kv,
   p.per_half = kv.per_head;
   p.max_tiles = (a.max_seqlen_q + kTileM - 1) / kTileM;
   p.sl2 = a.scale * 1.4426950408889634f;
+  p.fw = FusedWrite{};
+  if (a.k_new) {
+    p.fw.k_new = a.k_new;
+    p.fw.v_new = a.v_new;
+    p.fw.k_stride = a.k_stride;
+    p.fw.v_stride = a.v_stride;
+    p.fw.slots = a.slot_mapping;
+    p.fw.k_cache = a.k_cache;
+    p.fw.v_cache = a.v_cache;
+    p.fw.num_slots = static_cast<int64_t>(a.num_blocks) * kBlockSize;
+    p.fw.num_tokens = a.total_q;
+    p.fw.row_elems = a.num_kv_heads * kHeadDim;
+    p.fw.barrier = a.barrier_ws;
+  }
   // The warpgroups' register shares (setmaxnreg) add up to the launch's
   // total only if the kernel was built with exactly kRegsLaunch registers per
   // thread; with fewer, the softmax warpgroups' request could never be met.
@@ -1062,6 +1167,22 @@ cudaError_t launch_prefill_persistent(const PrefillArgs& a, const CacheMaps& kv,
   static std::atomic<int> smem_set[kMaxDevices];
   cudaError_t e = ensure_dyn_smem(prefill_persistent_kernel, kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
+  if (a.k_new) {
+    // Fused write: one CTA per SM (the write wants every SM's bandwidth), all
+    // resident at once -- a cooperative launch guarantees that or fails --
+    // since every CTA waits for every other at the grid barrier.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_persistent_kernel, qmap, kv.k, kv.v, omap, p);
+  }
   // One CTA per SM, or fewer when the launch bounds allow fewer items.
   const long long items = static_cast<long long>(a.num_seqs) * p.max_tiles * a.num_kv_heads * p.npairs;
   const int grid = static_cast<int>(std::min<long long>(num_sms, items));
