@@ -224,3 +224,22 @@ def test_prefill_understated_max_seqlen_q_long_prompt_is_flagged():
                            w.scale, 2100, w.max_seqlen_k)
     torch.cuda.synchronize()
     assert "LEN_RANGE" in pkv.device_error(clear=True)
+
+
+def test_prefill_many_sequences_fallback_order():
+    """1100 sequences, one with 33,000 cached tokens: the sorted item order
+    would take more than 8192 (level x 32-sequence) steps to enumerate, so the
+    persistent kernel's scheduler falls back to the "last query tile of each
+    sequence first" order.  Every row matches the oracle, and the output is
+    bit-identical to the one-CTA-per-tile kernel's."""
+    rng = np.random.default_rng(1100)
+    lens = [int(x) for x in rng.integers(1, 41, size=1099)] + [33130]
+    cached = [0] * 1099 + [33000]
+    nch = -(-len(lens) // 32)
+    vmax = -(-max(lens) // 128)
+    assert vmax * nch > 8192  # the fallback order is the one under test
+    need = sum(-(-L // 256) for L in lens)
+    w = W.make_prefill("fallback_order", 1100, lens, cached, 16, 8, num_blocks=need + 4)
+    run_prefill(w)
+    a, b = _prefill_both_kernels(w)
+    assert np.array_equal(a, b)
