@@ -295,23 +295,30 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // tcgen05.mma with the k-step's constant descriptor offsets added inside the
 // instruction sequence, so the issuing thread keeps only the base
 // descriptors in registers (a precomputed descriptor per k-step would hold
-// 32 registers in a warp that runs with 64).
+// 32 registers in a warp that runs with 64).  The offset lands in the 14-bit
+// start-address field (bits 0-13: shared-memory address / 16, below 2^14 for
+// any operand inside the CTA's shared memory), so it never carries out of the
+// low word and a 32-bit add is exact.
 template <uint32_t AOFF, uint32_t BOFF>
 __device__ __forceinline__ void mma_ss_at(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "n"(AOFF >> 4), "n"(BOFF >> 4)
+      "{\n\t.reg .pred p;\n\t.reg .b32 t, u;\n\t.reg .b64 a, b;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "add.u32 t, %1, %7;\n\tadd.u32 u, %3, %8;\n\t"
+      "mov.b64 a, {t, %2};\n\tmov.b64 b, {u, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d),
+      "r"(static_cast<uint32_t>(adesc)), "r"(static_cast<uint32_t>(adesc >> 32)),
+      "r"(static_cast<uint32_t>(bdesc)), "r"(static_cast<uint32_t>(bdesc >> 32)), "r"(idesc), "r"(acc),
+      "n"(AOFF >> 4), "n"(BOFF >> 4)
       : "memory");
 }
 template <uint32_t BOFF>
 __device__ __forceinline__ void mma_ts_at(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "add.s64 b, %2, %5;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %3, p;\n\t}" ::"r"(d),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc), "n"(BOFF >> 4)
+      "{\n\t.reg .pred p;\n\t.reg .b32 u;\n\t.reg .b64 b;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 u, %2, %6;\n\tmov.b64 b, {u, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(static_cast<uint32_t>(bdesc)), "r"(static_cast<uint32_t>(bdesc >> 32)), "r"(idesc),
+      "r"(acc), "n"(BOFF >> 4)
       : "memory");
 }
 
@@ -779,6 +786,19 @@ __device__ void run_softmax(const PrefillParams& p, const Smem& sm, int slot, in
         m_ref = m_new;
       }
       const float mu = m_ref;  // finite: key 0 is visible to every row
+      // p = 2^(s * scale * log2e - m), packed to bf16 pairs in registers
+      // before the wait below, so that the exponentials overlap the previous
+      // tile's P V (keys 32q..32q+31 go to columns 16q..16q+15).
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sl2 = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
+      uint32_t pk[64];
+#pragma unroll
+      for (int x = 0; x < 128; x += 2) {
+        const float2 a = ffma2(make_float2(s[x], s[x + 1]), sl2, nmu);
+        const float2 ex = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+        rs[(x >> 1) & 3] = fadd2(rs[(x >> 1) & 3], ex);
+        pk[x >> 1] = pack_bf16x2(ex.x, ex.y);
+      }
       // P_X of the previous tile must be consumed (and O_X stable) before
       // this tile's P_X is stored.
       if (gt > 0) {
@@ -788,23 +808,8 @@ __device__ void run_softmax(const PrefillParams& p, const Smem& sm, int slot, in
         }
         tc::fence_after();
       }
-      // p = 2^(s * scale * log2e - m), packed to bf16 pairs and stored in
-      // this slot's P columns 32 keys at a time (keys 32q..32q+31 go to
-      // columns 16q..16q+15).
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      const float2 sl2 = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const float2 a = ffma2(make_float2(s[32 * q + x], s[32 * q + x + 1]), sl2, nmu);
-          const float2 ex = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-          rs[(x >> 1) & 3] = fadd2(rs[(x >> 1) & 3], ex);
-          pk[x >> 1] = pack_bf16x2(ex.x, ex.y);
-        }
-        tc::st16u(p_addr + 16 * q, pk);
-      }
+      for (int q = 0; q < 4; ++q) tc::st16u(p_addr + 16 * q, pk + 16 * q);
       // O_X is stable here: P V_X of the previous tile has completed.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
