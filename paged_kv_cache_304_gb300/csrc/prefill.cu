@@ -456,6 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
       }
       const float mu = m_ref;  // finite: key 0 is visible to every row
+      // p = 2^(s * scale * log2e - m), packed to bf16 pairs; the first
+      // 64 keys before the wait below (their exponentials overlap PV_X(j-1)),
+      // the rest after it (keys 32q..32q+31 go to columns 16q..16q+15).
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sl2 = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
+      uint32_t pk[64];
+#pragma unroll
+      for (int x = 0; x < 64; x += 2) {
+        const float2 a = ffma2(make_float2(s[x], s[x + 1]), sl2, nmu);
+        const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+        rs[(x >> 1) & 3] = fadd2(rs[(x >> 1) & 3], e);
+        pk[x >> 1] = pack_bf16x2(e.x, e.y);
+      }
       // P_X(j-1) must be consumed (and O_X stable) before P_X(j) is stored.
       if (j > 0) {
         if (!mbar_wait(&sm.pv_done[slot], (j - 1) & 1, &g_err_prefill)) {
@@ -464,22 +477,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after();
       }
-      // p = 2^(s * scale * log2e - m), packed to bf16 pairs and stored in
-      // this slot's P columns 32 keys at a time (keys 32q..32q+31 go to
-      // columns 16q..16q+15).
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      const float2 sl2 = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
+      for (int q = 0; q < 2; ++q) tc::st16u(p_addr + 16 * q, pk + 16 * q);
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const float2 a = ffma2(make_float2(s[32 * q + x], s[32 * q + x + 1]), sl2, nmu);
+      for (int q = 2; q < 4; ++q) {
+#pragma unroll
+        for (int x = 32 * q; x < 32 * q + 32; x += 2) {
+          const float2 a = ffma2(make_float2(s[x], s[x + 1]), sl2, nmu);
           const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
           rs[(x >> 1) & 3] = fadd2(rs[(x >> 1) & 3], e);
           pk[x >> 1] = pack_bf16x2(e.x, e.y);
         }
-        tc::st16u(p_addr + 16 * q, pk);
+        tc::st16u(p_addr + 16 * q, pk + 16 * q);
       }
       // O_X is stable here: PV_X(j-1) has completed (pv_done above).
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
