@@ -31,9 +31,10 @@
 //   32 (w % 4) .. +31, so thread r of a group owns query row r (TMEM lane
 //   r).  It loads its 128 scores with tcgen05.ld, releases the S columns,
 //   applies the causal mask on diagonal tiles, keeps the running row maximum
-//   (log2 units, scale * log2(e) folded in), waits for the previous P V of
-//   its slot, rescales O in tensor memory only when the maximum grew by
-//   more than 2^8, and stores P.  At the end it normalises O by the row sum
+//   (log2 units, scale * log2(e) folded in), computes the first 64
+//   probabilities, waits for the previous P V of its slot, stores them and
+//   the other 64, and rescales O in tensor memory only when the maximum grew
+//   by more than 2^8.  At the end it normalises O by the row sum
 //   and stages the bf16 rows in the Q buffer in the layout of a TMA box; a
 //   warp whose 32 rows all belong to the sequence stores them with bulk
 //   tensor copies, a warp holding the sequence's end writes its rows with

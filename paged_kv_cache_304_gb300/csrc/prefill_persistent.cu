@@ -41,9 +41,11 @@
 //     P_A | P_B (64 columns each, packed bf16) and O_A | O_B (128 each).
 // * WG1 / WG2 (176 registers): softmax of slot A / B; thread r owns query row
 //   r (TMEM lane r): scores read with tcgen05.ld, S columns released, causal
-//   mask on diagonal tiles, running maximum in log2 units, O rescaled in
-//   tensor memory only when the maximum grew by more than 2^8, P stored; the
-//   row sum goes to the epilogue through shared memory.
+//   mask on diagonal tiles, running maximum in log2 units, all 128
+//   probabilities packed in registers before the wait for the slot's
+//   previous P V, then P stored and O rescaled in tensor memory only when the
+//   maximum grew by more than 2^8; the row sum goes to the epilogue through
+//   shared memory.
 // * WG3 (96 registers): epilogue; per item and slot it reads O (after which the
 //   slot's next P V may overwrite it), normalises by the row sum and writes
 //   the bf16 rows through the staging entry (bulk tensor stores for warps
