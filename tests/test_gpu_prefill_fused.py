@@ -54,6 +54,24 @@ def test_fused_prefill_equals_separate_and_oracle(name):
     assert pkv.device_error() == []
 
 
+@pytest.mark.parametrize("hq,hkv", [(12, 4), (8, 8), (16, 1)])
+def test_fused_prefill_group_sizes(hq, hkv):
+    """Groups of 3 (a head pair plus a lone head: items without slot B), 1
+    and 16, with a continuation chunk, prefix hits and a 1-token sequence:
+    bit-identical to the separate calls, caches bit-exact, close to the oracle."""
+    w = W.make_prefill(f"fused_g{hq}_{hkv}", 933 + hq + hkv, [700, 300, 1000, 129, 1], [200, 0, 513, 0, 0], hq,
+                       hkv, num_blocks=24)
+    o1, o2, c1, c2 = _both(w)
+    assert torch.equal(c1[0], c2[0]) and torch.equal(c1[1], c2[1]), "caches differ"
+    assert torch.equal(o1, o2), "outputs differ"
+    okc, ovc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_cache_write(w.k_new, w.v_new, w.slot_mapping, okc, ovc)
+    assert np.array_equal(to_host(c2[0]), okc) and np.array_equal(to_host(c2[1]), ovc), "write not bit-exact"
+    ref = oracle.paged_attn_prefill(w.q, okc, ovc, w.cu_seqlens_q, w.cu_seqlens_k, w.block_tables, w.scale)
+    check_close(to_host(o2), ref, f"fused prefill hq={hq} hkv={hkv}")
+    assert pkv.device_error() == []
+
+
 def test_fused_prefill_reuses_its_workspace_and_skips_pad_slots():
     """One workspace across several calls (the barrier leaves it ready), a
     tiny batch (fewer work items than SMs), and slot -1 rows left unwritten."""
