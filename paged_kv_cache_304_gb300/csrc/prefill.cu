@@ -163,10 +163,13 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const CUten
 
 // Matrix descriptors are built once per CTA; a k-step only adds a constant to
 // the 16-byte address field in the low bits (the addresses stay below
-// 256 KiB, so the add never carries out of the field).  Rebuilding the 64-bit
+// 256 KiB, so the add never carries out of the field, nor out of the low
+// word: one 32-bit add, the high word kept as it is).  Rebuilding the 64-bit
 // descriptor for every instruction made the single issuing thread, not the
 // tensor pipe, the limit.
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + (bytes >> 4));
+}
 
 // Bulk tensor store of one box from shared memory, tracked by the bulk
 // async-group of the issuing thread.
