@@ -242,10 +242,13 @@ PKV_API pkv_status pkv_paged_attn_prefill(const pkv_bf16* q, const pkv_bf16* k_c
  *                  when allocated); every call leaves it ready for the next.
  *                  Two calls that may run concurrently need two workspaces.
  *                  If a call reports PKV_DEVERR_WAIT_TIMEOUT, zero it again.
- * Every other argument is as in pkv_paged_attn_prefill.  The call always uses
- * the persistent kernel (one CTA per SM, launched cooperatively so that all of
- * them are resident at the barrier); a launch that cannot be co-resident
- * returns PKV_ERR_CUDA.
+ * Every other argument is as in pkv_paged_attn_prefill.  Up to a stated
+ * max_seqlen_q of 2048 the call uses the persistent kernel (one CTA per SM,
+ * launched cooperatively so that all of them are resident at the barrier); a
+ * launch that cannot be co-resident returns PKV_ERR_CUDA.  Above 2048 it
+ * launches the KV write and then the long-prompt attention kernel on the
+ * stream (two launches, faster there) and leaves the workspace untouched;
+ * the results are the same either way.
  */
 PKV_API size_t pkv_prefill_fused_workspace_bytes(void);
 PKV_API pkv_status pkv_paged_attn_prefill_fused_write(

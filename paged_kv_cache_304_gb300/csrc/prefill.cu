@@ -589,7 +589,22 @@ cudaError_t launch_paged_attn_prefill(const PrefillArgs& a, const CacheMaps& kv,
   // the tile's tensor work, so they go to the persistent kernel.
   // The fused KV write needs every CTA resident at once (a grid barrier
   // separates the write from the first cache read): also the persistent kernel.
-  if (a.max_seqlen_q <= kPersistentMaxSeqlenQ || a.k_new) return launch_prefill_persistent(a, kv, qmap, omap, num_sms, stream);
+  if (a.max_seqlen_q <= kPersistentMaxSeqlenQ) return launch_prefill_persistent(a, kv, qmap, omap, num_sms, stream);
+  if (a.k_new) {
+    // Long prompts: the write costs the same as its own kernel, and this
+    // kernel is faster than the persistent one there.  The attention kernel's
+    // dependent-launch wait orders its cache reads after the write.
+    cudaError_t e = launch_kv_cache_write(a.k_new, a.k_stride, a.v_new, a.v_stride, a.slot_mapping, a.total_q,
+                                          a.k_cache, a.v_cache, static_cast<int64_t>(a.num_blocks) * kBlockSize,
+                                          a.num_kv_heads * kHeadDim, stream);
+    if (e != cudaSuccess) return e;
+    PrefillArgs b = a;
+    b.k_new = b.v_new = nullptr;
+    b.slot_mapping = nullptr;
+    b.k_cache = b.v_cache = nullptr;
+    b.barrier_ws = nullptr;
+    return launch_paged_attn_prefill(b, kv, qmap, omap, num_sms, stream);
+  }
   PrefillParams p;
   p.cu_q = a.cu_seqlens_q;
   p.cu_k = a.cu_seqlens_k;

@@ -2,10 +2,12 @@
 
 pkv_paged_attn_prefill_fused_write writes every new token's K/V row into the
 cache (each SM a share), waits at a grid-wide barrier, then runs the
-persistent prefill kernel.  The writes are the standalone write's bytes and
-the attention is the same per-tile arithmetic as either prefill kernel, so
-outputs and caches must be bitwise identical to kv_cache_write followed by
-paged_attn_prefill, and within tolerance of the fp64 oracle.
+persistent prefill kernel; above a stated max_seqlen_q of 2048 it launches
+the write kernel and then the long-prompt kernel.  The writes are the
+standalone write's bytes and the attention is the same per-tile arithmetic
+as either prefill kernel, so outputs and caches must be bitwise identical to
+kv_cache_write followed by paged_attn_prefill, and within tolerance of the
+fp64 oracle.
 """
 
 import numpy as np
@@ -97,5 +99,26 @@ def test_fused_prefill_out_of_range_slot_is_flagged():
     pkv.paged_attn_prefill_fused_write(to_dev(w.q), to_dev(w.k_new), to_dev(w.v_new), i32(slots), kc, vc,
                                        i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables), w.scale,
                                        w.max_seqlen_q, w.max_seqlen_k)
+    torch.cuda.synchronize()
+    assert "SLOT_RANGE" in pkv.device_error(clear=True)
+
+
+def test_fused_prefill_long_prompt_path_flags_bad_slot_and_leaves_workspace():
+    """Above a stated max_seqlen_q of 2048 (two launches): bit-identical to the
+    separate calls, an out-of-range slot is flagged by the write, and the
+    workspace is not touched."""
+    w = W.make_prefill("fused_long", 934, [3000, 700], [0, 100], 16, 8, num_blocks=20)
+    ws = pkv.prefill_fused_workspace(torch.device("cuda:0"))
+    ws.fill_(7)
+    o1, o2, c1, c2 = _both(w, workspace=ws)
+    assert torch.equal(c1[0], c2[0]) and torch.equal(c1[1], c2[1]) and torch.equal(o1, o2)
+    assert bool((ws == 7).all())
+    assert pkv.device_error() == []
+    slots = w.slot_mapping.copy()
+    slots[11] = 20 * 256 + 5  # beyond the pool
+    kc, vc = to_dev(w.k_cache), to_dev(w.v_cache)
+    pkv.paged_attn_prefill_fused_write(to_dev(w.q), to_dev(w.k_new), to_dev(w.v_new), i32(slots), kc, vc,
+                                       i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.block_tables), w.scale,
+                                       w.max_seqlen_q, w.max_seqlen_k, workspace=ws)
     torch.cuda.synchronize()
     assert "SLOT_RANGE" in pkv.device_error(clear=True)
