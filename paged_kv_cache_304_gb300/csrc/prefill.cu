@@ -51,7 +51,8 @@
 // complete (bounded waits on their barriers), frees its tensor memory and
 // returns.
 //
-// This grid form is used for long prompts (stated max_seqlen_q above 2048);
+// This grid form is used for long prompts (stated max_seqlen_q above 2048),
+// also after the KV write kernel when the call has the write fused in;
 // batches of short query tiles go to the persistent kernel in
 // prefill_persistent.cu, which computes the same tiles in the same order.
 #include <cuda_runtime.h>
